@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs for the KDA decode step and the chunked prefill.
+
+This module only draws random numbers and packs them into the storage formats
+the library consumes (BF16 bit patterns, FP32). It holds none of the method's
+arithmetic: no convolution, no normalisation, no state update. Both the CPU
+oracle (test infrastructure) and the CUDA path take their inputs from here, so
+the two always see bit-identical data.
+
+Distributions follow the GLM-5.3-Flash decode workload described on the source
+pages (64 heads x 128 x 128 state, kernel-4 short convolution):
+
+* pre-conv q, k, v ~ N(0, 1), rounded to BF16 (round to nearest even);
+* conv weights ~ N(0, 0.5^2) in FP32, layout [3, D, 4] (tap 3 = current token);
+* conv cache ~ N(0, 1) rounded to BF16, layout [M, 3, 3, D] (tap 0 = oldest);
+* beta = sigmoid(N(0, 1)) per head, FP32;
+* alpha = sigmoid(N(2, 1)) per key channel, FP32 (linear-space decay);
+* initial state S0 ~ N(0, 0.1^2), rounded to BF16 and widened to FP32, so that
+  FP32 and BF16 state storage start from identical values.
+
+Draw order for a decode layer: conv_w, conv cache, S0, then per step
+(x, beta_raw, alpha_raw).  Draw order for a prefill problem: S0, q, k, v,
+beta_raw, alpha_raw.  The generator is numpy's PCG64 (``default_rng``).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_bits",
+    "bf16_widen",
+    "decode_layer",
+    "prefill_problem",
+    "layer_seed",
+]
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """FP32 array -> BF16 bit patterns (uint16), round to nearest even.
+
+    Inputs here are finite normal draws, so no NaN handling is needed.
+    """
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    return ((b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_widen(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns (uint16) -> the exactly equal FP32 values."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _sigmoid32(z: np.ndarray) -> np.ndarray:
+    # input-distribution shaping only (beta and alpha are drawn as sigmoid of
+    # a normal); evaluated in float64 and stored as FP32
+    return (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+
+
+def layer_seed(config: int, layer: int) -> int:
+    """Per-layer seed: 1000 * config + layer."""
+    return 1000 * config + layer
+
+
+def decode_layer(seed: int, M: int, H: int = 64, d: int = 128, T: int = 1,
+                 alpha_mean: float = 2.0) -> dict:
+    """Inputs for T consecutive decode steps of one KDA layer.
+
+    Returns a dict with
+      conv_w      float32 [3, D, 4]
+      cache_bits  uint16  [M, 3, 3, D]   (BF16)   cache_f32: widened copy
+      S0          float32 [M, H, d, d]   (BF16-representable values)
+      x_bits      list of T uint16 [M, 3, D]      x_f32: widened copies
+      beta        list of T float32 [M, H]
+      alpha       list of T float32 [M, H, d]
+    with D = H * d.
+    """
+    rng = np.random.default_rng(seed)
+    D = H * d
+    conv_w = (rng.standard_normal((3, D, 4)) * 0.5).astype(np.float32)
+    cache_bits = bf16_bits(rng.standard_normal((M, 3, 3, D)).astype(np.float32))
+    S0 = bf16_widen(bf16_bits((rng.standard_normal((M, H, d, d)) * 0.1).astype(np.float32)))
+    x_bits, beta, alpha = [], [], []
+    for _ in range(T):
+        x_bits.append(bf16_bits(rng.standard_normal((M, 3, D)).astype(np.float32)))
+        beta.append(_sigmoid32(rng.standard_normal((M, H))))
+        alpha.append(_sigmoid32(rng.standard_normal((M, H, d)) + alpha_mean))
+    return {
+        "M": M, "H": H, "d": d, "T": T,
+        "conv_w": conv_w,
+        "cache_bits": cache_bits,
+        "cache_f32": bf16_widen(cache_bits),
+        "S0": np.ascontiguousarray(S0),
+        "x_bits": x_bits,
+        "x_f32": [bf16_widen(b) for b in x_bits],
+        "beta": beta,
+        "alpha": alpha,
+    }
+
+
+def prefill_problem(seed: int, M: int, T: int, H: int = 64, d: int = 128,
+                    alpha_mean: float = 2.0) -> dict:
+    """Inputs for a chunked prefill of T tokens (post-conv q, k, v).
+
+    Returns q_bits/k_bits/v_bits uint16 [M, T, H, d] (BF16) with widened
+    float32 copies q/k/v, alpha float32 [M, T, H, d], beta float32 [M, T, H]
+    and S0 float32 [M, H, d, d] (BF16-representable values).
+    """
+    rng = np.random.default_rng(seed)
+    S0 = bf16_widen(bf16_bits((rng.standard_normal((M, H, d, d)) * 0.1).astype(np.float32)))
+    out = {"M": M, "T": T, "H": H, "d": d, "S0": np.ascontiguousarray(S0)}
+    for name in ("q", "k", "v"):
+        bits = bf16_bits(rng.standard_normal((M, T, H, d), dtype=np.float32))
+        out[name + "_bits"] = bits
+        out[name] = bf16_widen(bits)
+    out["beta"] = _sigmoid32(rng.standard_normal((M, T, H)))
+    out["alpha"] = _sigmoid32(rng.standard_normal((M, T, H, d), dtype=np.float32) + alpha_mean)
+    return out

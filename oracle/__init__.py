@@ -1,0 +1,196 @@
+"""KDA oracle — TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, float64 CPU statement of what the KDA decode step and the
+chunked prefill compute. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. It shares no code
+with the CUDA library and never imports it; both sides take their inputs from
+``linear_attention_decode_step_gb300.inputs``.
+
+Two parts:
+
+* ``kda_oracle.c`` (loaded through ctypes): the short conv + SiLU and the
+  sequential recurrence, in the order of the pages' four decode steps
+  ("GLM-5.3 deep dive", 8.2.3 Eq. 1 and 8.2.6).
+* ``chunk_prefill`` below (numpy): the chunkwise-parallel WY / UT form of the
+  same recurrence ("GLM-5.3 deep dive", 8.2.5, Eq. 6-9), written step by step
+  in the page's order with numpy matmuls as the only library primitive.
+
+Every function is pinned by tests that do not reuse its code; nothing here is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+__all__ = [
+    "build",
+    "conv_step",
+    "recurrent",
+    "decode_step",
+    "chunk_prefill",
+    "L2_EPS",
+]
+
+#: eps inside the root of the L2 normalisation ("GLM-5.3 deep dive", 8.2.6,
+#: implementation notes: epsilon 1e-6)
+L2_EPS = 1e-6
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_SO = os.path.join(_HERE, "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile kda_oracle.c into libkda_oracle.so next to it (plain gcc)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def bind(path: str):
+    """Load a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(ctypes.c_double)
+    I, Dd = ctypes.c_int, ctypes.c_double
+    lib.kda_oracle_conv_step.argtypes = [P, P, P, P, I, I]
+    lib.kda_oracle_recurrent.argtypes = [P, P, P, P, P, P, P,
+                                         I, I, I, I, I, Dd, I, Dd]
+    lib.kda_oracle_decode_step.argtypes = [P, P, P, P, P, P, P,
+                                           I, I, I, Dd, Dd]
+    for f in (lib.kda_oracle_conv_step, lib.kda_oracle_recurrent,
+              lib.kda_oracle_decode_step):
+        f.restype = None
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = bind(build())
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.array(a, dtype=np.float64, order="C", copy=True)
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def conv_step(x, w, cache):
+    """Short conv + SiLU for one token.
+
+    x [M,3,D], w [3,D,4], cache [M,3,3,D] -> (y [M,3,D], new cache).
+    Inputs are not modified.
+    """
+    x, w, cache = _f64(x), _f64(w), _f64(cache)
+    M, three, D = x.shape
+    assert three == 3 and w.shape == (3, D, 4) and cache.shape == (M, 3, 3, D)
+    y = np.empty_like(x)
+    _load().kda_oracle_conv_step(_p(x), _p(w), _p(cache), _p(y), M, D)
+    return y, cache
+
+
+def recurrent(q, k, v, alpha, beta, S0, scale=1.0, use_l2norm=True, eps=L2_EPS):
+    """Sequential KDA recurrence over T tokens.
+
+    q, k, alpha [M,T,H,dk]; v [M,T,H,dv]; beta [M,T,H]; S0 [M,H,dk,dv]
+    -> (o [M,T,H,dv], S [M,H,dk,dv]). Inputs are not modified.
+    """
+    q, k, v, alpha, beta, S = (_f64(a) for a in (q, k, v, alpha, beta, S0))
+    M, T, H, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and alpha.shape == q.shape
+    assert v.shape == (M, T, H, dv) and beta.shape == (M, T, H)
+    assert S.shape == (M, H, dk, dv)
+    o = np.empty((M, T, H, dv), dtype=np.float64)
+    _load().kda_oracle_recurrent(_p(q), _p(k), _p(v), _p(alpha), _p(beta),
+                                 _p(S), _p(o), M, T, H, dk, dv, float(scale),
+                                 1 if use_l2norm else 0, float(eps))
+    return o, S
+
+
+def decode_step(x, w, cache, alpha, beta, S0, scale=1.0, eps=L2_EPS):
+    """One fused decode step of a KDA layer (conv + SiLU, L2 norm, Eq. 1, read).
+
+    x [M,3,D]; w [3,D,4]; cache [M,3,3,D]; alpha [M,H,d]; beta [M,H];
+    S0 [M,H,d,d] -> (o [M,H,d], S [M,H,d,d], cache [M,3,3,D]).
+    """
+    x, w, cache, alpha, beta, S = (_f64(a) for a in (x, w, cache, alpha, beta, S0))
+    M, H, d, d2 = S.shape
+    assert d == d2 and x.shape == (M, 3, H * d) and alpha.shape == (M, H, d)
+    assert beta.shape == (M, H) and cache.shape == (M, 3, 3, H * d)
+    o = np.empty((M, H, d), dtype=np.float64)
+    _load().kda_oracle_decode_step(_p(x), _p(w), _p(cache), _p(alpha), _p(beta),
+                                   _p(S), _p(o), M, H, d, float(scale), float(eps))
+    return o, S, cache
+
+
+def _l2norm_rows(x, eps):
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _unit_lower_solve(A, B):
+    """X = (I + A)^{-1} B for strictly lower-triangular A, by forward
+    substitution, one row after another (the page's UT-transform inverse)."""
+    X = np.array(B, dtype=np.float64, copy=True)
+    for r in range(X.shape[0]):
+        X[r] -= A[r, :r] @ X[:r]
+    return X
+
+
+def chunk_prefill(q, k, v, alpha, beta, S0, chunk=64, scale=1.0,
+                  use_l2norm=True, eps=L2_EPS):
+    """Chunkwise-parallel (WY / UT transform) KDA prefill, float64.
+
+    Follows "GLM-5.3 deep dive", 8.2.5, per chunk of C tokens with incoming
+    state S and, per key channel, the cumulative log-decay G (inclusive:
+    G_r = sum_{m<=r} log alpha_m, so Gamma = exp(G)):
+      Eq. 6: M = (I + StrictTril(Diag(beta) (Gamma*K) (K/Gamma)^T))^{-1} Diag(beta)
+      Eq. 7: W = M (Gamma*K),  U = M V
+      Eq. 8: S_next = Diag(gamma^C) S + (Gamma^{i->C} * K)^T (U - W S)
+      Eq. 9: O = (Gamma*Q) S + Tril((Gamma*Q)(K/Gamma)^T) (U - W S)
+    where gamma^C = exp(G_C) and Gamma^{i->C} = exp(G_C - G_i).
+
+    Domain: exp(+-G) must stay finite in float64, i.e. the summed log-decay
+    over one chunk must stay above about -700 per channel.
+
+    Shapes as in ``recurrent``; returns (o, S).
+    """
+    q, k, v, alpha, beta, S = (_f64(a) for a in (q, k, v, alpha, beta, S0))
+    M, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if use_l2norm:
+        q, k = _l2norm_rows(q, eps), _l2norm_rows(k, eps)
+    o = np.zeros((M, T, H, dv), dtype=np.float64)
+    for m in range(M):
+        for h in range(H):
+            Sh = S[m, h]
+            for c0 in range(0, T, chunk):
+                c1 = min(c0 + chunk, T)
+                Q, K, V = q[m, c0:c1, h], k[m, c0:c1, h], v[m, c0:c1, h]
+                b = beta[m, c0:c1, h]
+                G = np.cumsum(np.log(alpha[m, c0:c1, h]), axis=0)
+                Kd = np.exp(G) * K          # Gamma (.) K
+                Ki = K * np.exp(-G)         # K / Gamma
+                Qd = np.exp(G) * Q          # Gamma (.) Q
+                A = np.tril(b[:, None] * (Kd @ Ki.T), -1)
+                Mx = _unit_lower_solve(A, np.diag(b))
+                W, U = Mx @ Kd, Mx @ V
+                Delta = U - W @ Sh
+                o[m, c0:c1, h] = scale * (Qd @ Sh + np.tril(Qd @ Ki.T) @ Delta)
+                Sh = np.exp(G[-1])[:, None] * Sh + (np.exp(G[-1] - G) * K).T @ Delta
+            S[m, h] = Sh
+    return o, S

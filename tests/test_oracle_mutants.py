@@ -1,0 +1,69 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle's C source (a
+dropped term, a wrong sign or index, a step out of order), builds it, swaps it
+in for the real oracle and checks that at least one pin in test_oracle.py
+fails. Everything runs on the CPU; the real oracle is restored afterwards.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "kda_oracle.c")
+
+MUTANTS = {
+    "scalar_fade": ("Sh[(size_t)i * dv + j] *= a[i];", "Sh[(size_t)i * dv + j] *= a[0];"),
+    "no_fade": ("Sh[(size_t)i * dv + j] *= a[i];", "(void)a;"),
+    "error_sign": ("b * (v[tv + j] - u[j])", "b * (u[j] - v[tv + j])"),
+    "no_beta": ("kn[i] * b * (v[tv + j] - u[j])", "kn[i] * (v[tv + j] - u[j])"),
+    "predict_with_q": ("acc += kn[i] * Sh[(size_t)i * dv + j];\n                    u[j] = acc;",
+                       "acc += qn[i] * Sh[(size_t)i * dv + j];\n                    u[j] = acc;"),
+    "read_with_k": ("acc += qn[i] * Sh[(size_t)i * dv + j];\n                    o[tv + j]",
+                    "acc += kn[i] * Sh[(size_t)i * dv + j];\n                    o[tv + j]"),
+    "eps_outside_root": ("1.0 / sqrt(sq + eps)", "1.0 / (sqrt(sq) + eps)"),
+    "scale_dropped": ("o[tv + j] = scale * acc;", "o[tv + j] = acc;"),
+    "conv_taps_reversed": ("wc[0] * c0[c] + wc[1] * c1[c] + wc[2] * c2[c]\n                           + wc[3] * xt[c]",
+                           "wc[3] * c0[c] + wc[2] * c1[c] + wc[1] * c2[c]\n                           + wc[0] * xt[c]"),
+    "conv_no_silu": ("yt[c] = silu(pre);", "yt[c] = pre;"),
+    "cache_not_shifted": ("c0[c] = c1[c];", "c0[c] = c0[c];"),
+}
+
+PINS = [
+    pins.test_worked_example_states,
+    pins.test_worked_example_reads,
+    pins.test_worked_example_half_beta,
+    lambda: pins.test_brute_force_dense_product(3, 8),
+    lambda: pins.test_brute_force_dense_product(8, 3),
+    pins.test_l2norm_eps_inside_root,
+    pins.test_alpha1_beta0_leaves_state_and_reads_it,
+    pins.test_beta1_unit_key_reads_back_value,
+    pins.test_beta0_fades_each_row_by_its_alpha,
+    pins.test_erase_shrinks_only_along_key,
+    pins.test_scale_is_linear_on_output_only,
+    pins.test_conv_identity_weights_is_silu,
+    pins.test_conv_matches_direct_causal_convolution,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + name
+    bad = tmp_path / "mutant.c"
+    bad.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", str(bad),
+                           "-o", str(so), "-lm"])
+    monkeypatch.setattr(oracle, "_lib", oracle.bind(str(so)))
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(getattr(pin, "__name__", "pin"))
+    assert caught, "no pin caught mutant " + name
