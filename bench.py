@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""KDA decode benchmark on GB300: state GB/s and ms/layer at M=32, FP32 state.
+
+One step is one token through a 34-layer KDA decode stack (GLM-5.3-Flash has
+34 KDA layers): 34 launches of the fused decode kernel (conv + SiLU, L2 norm,
+Eq. 1 update, readout), each on its own layer's state and conv cache, with
+M = 32 streams x 64 heads x 128 x 128 FP32 state (134 MB per layer; 4.6 GB
+touched per step, so every layer's state comes from HBM, not L2).
+
+Printed (rank 0, one JSON line): value = state GB/s (2 * state bytes per
+layer per step / time), ms_per_step, ms_per_layer, the roofline of the
+decode kernel against the measured HBM peak, an end-to-end number through the
+public API with per-step host<->device copies, the SM clocks seen during the
+timed region, and the fp64 CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N --steps K --warmup W]        this library
+  python bench.py --impl reference [...]                  the CPU oracle
+Multi-GPU (torchrun, one rank per GPU): independent replicas, weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA decode state GB/s & ms/layer at M=32 FP32 (fraction of GB300 HBM peak)"
+UNIT = "GB/s"
+H, DH = 64, 128
+LAYERS = 34
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "linear_attention_decode_step_gb300", "csrc", "kda_decode.cu")
+TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_decode_M32_f32.md")
+
+
+# --------------------------------------------------------------------------- sizes
+def dtype_size(name: str) -> int:
+    return 2 if name == "bf16" else 4
+
+
+def state_bytes_per_launch(M: int, state_dtype: str) -> int:
+    """State read + write of one layer: 2 * M * H * dk * dv * sizeof(state)."""
+    return 2 * M * H * DH * DH * dtype_size(state_dtype)
+
+
+def algorithmic_bytes_per_launch(M: int, state_dtype: str, x_dtype: str) -> int:
+    """Every byte one launch must move at least once.
+
+    Per (stream, head): state read + write 2*dk*dv*s, pre-conv q/k/v 3*d*x,
+    conv cache read + write 2*9*d*x, alpha 4*d, beta 4, o 4*d. Per launch:
+    conv weights 3*H*d*4*4 (shared by all streams).
+    """
+    s, x = dtype_size(state_dtype), dtype_size(x_dtype)
+    per_unit = 2 * DH * DH * s + 3 * DH * x + 18 * DH * x + 4 * DH + 4 + 4 * DH
+    return M * H * per_unit + 3 * H * DH * 16
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic_per_launch():
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch from the
+    committed ncu summary, if it was taken on the current decode kernel."""
+    try:
+        text = open(TRAFFIC_NOTE).read()
+    except OSError:
+        return None
+    src = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != src:
+        return None
+    return float(m_tr.group(1))
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id, self.proc, self.path = gpu_id, None, None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["--id=" + self.gpu_id]
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        for line in open(self.path):
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------- workload
+class DecodeStack:
+    """L independent KDA layers resident on one GPU, with pinned host
+    mirrors of the per-step inputs and outputs for the end-to-end leg."""
+
+    def __init__(self, torch, kda, inputs, M, L, state_dtype, x_dtype, device, seed_cfg=3):
+        self.torch, self.kda, self.M, self.L = torch, kda, M, L
+        self.state_dtype, self.x_dtype = state_dtype, x_dtype
+        D = H * DH
+        xt = torch.bfloat16 if x_dtype == "bf16" else torch.float32
+        st = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+        # per-step inputs of all layers in one buffer each (one copy per step)
+        self.x = torch.empty((L, M, 3, D), dtype=xt, device=device)
+        self.alpha = torch.empty((L, M, H, DH), dtype=torch.float32, device=device)
+        self.beta = torch.empty((L, M, H), dtype=torch.float32, device=device)
+        self.o = torch.empty((L, M, H, DH), dtype=torch.float32, device=device)
+        self.conv_w, self.cache, self.state = [], [], []
+        self.host0 = None
+        for l in range(L):
+            inp = inputs.decode_layer(inputs.layer_seed(seed_cfg, l), M=M, T=1)
+            if l == 0:
+                self.host0 = inp
+            if x_dtype == "bf16":
+                self.x[l].copy_(torch.from_numpy(inp["x_bits"][0].view(np.int16)).view(torch.bfloat16))
+                cache = torch.from_numpy(inp["cache_bits"].view(np.int16)).to(device).view(torch.bfloat16)
+            else:
+                self.x[l].copy_(torch.from_numpy(inp["x_f32"][0]))
+                cache = torch.from_numpy(inp["cache_f32"]).to(device)
+            self.alpha[l].copy_(torch.from_numpy(inp["alpha"][0]))
+            self.beta[l].copy_(torch.from_numpy(inp["beta"][0]))
+            self.conv_w.append(torch.from_numpy(inp["conv_w"]).to(device))
+            self.cache.append(cache)
+            self.state.append(torch.from_numpy(inp["S0"]).to(device).to(st))
+        self.x_h = self.x.cpu().pin_memory()
+        self.alpha_h = self.alpha.cpu().pin_memory()
+        self.beta_h = self.beta.cpu().pin_memory()
+        self.o_h = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
+        self.stream = torch.cuda.Stream(device=device)
+        self.lib = kda.lib()
+        sp = self.stream.cuda_stream
+        xd = kda.KDA_BF16 if x_dtype == "bf16" else kda.KDA_F32
+        sd = kda.KDA_BF16 if state_dtype == "bf16" else kda.KDA_F32
+        # marshalled C-ABI arguments of each layer's kda_decode_step call
+        self.calls = [(self.x[l].data_ptr(), xd, self.conv_w[l].data_ptr(),
+                       self.cache[l].data_ptr(), xd, self.alpha[l].data_ptr(),
+                       self.beta[l].data_ptr(), self.state[l].data_ptr(), sd, 1.0,
+                       self.o[l].data_ptr(), M, H, DH, DH, sp) for l in range(L)]
+
+    def launch(self, l: int):
+        st = self.lib.kda_decode_step(*self.calls[l])
+        if st != 0:
+            raise self.kda.KdaError("kda_decode_step", st)
+
+    def step(self):
+        for l in range(self.L):
+            self.launch(l)
+
+    def copy_in(self):
+        self.x.copy_(self.x_h, non_blocking=True)
+        self.alpha.copy_(self.alpha_h, non_blocking=True)
+        self.beta.copy_(self.beta_h, non_blocking=True)
+
+    def copy_out(self):
+        self.o_h.copy_(self.o, non_blocking=True)
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.x_h, self.alpha_h, self.beta_h))
+
+    def d2h_bytes(self) -> int:
+        return self.o_h.numel() * self.o_h.element_size()
+
+
+def time_device(stack: DecodeStack, K: int, W: int, barrier):
+    """K steps with inputs resident; an event pair around every launch."""
+    torch = stack.torch
+    with torch.cuda.stream(stack.stream):
+        for _ in range(W):
+            stack.step()
+        torch.cuda.synchronize()
+        n = K * stack.L
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        barrier()
+        torch.cuda.synchronize()
+        i = 0
+        for _ in range(K):
+            for l in range(stack.L):
+                ev0[i].record(stack.stream)
+                stack.launch(l)
+                ev1[i].record(stack.stream)
+                i += 1
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = ev0[0].elapsed_time(ev1[-1])
+    launch_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    return total_ms, launch_ms
+
+
+def time_e2e(stack: DecodeStack, K: int, W: int, barrier):
+    """K steps through the public API: pinned host inputs copied in, 34
+    launches, outputs copied back, every step."""
+    torch = stack.torch
+    with torch.cuda.stream(stack.stream):
+        for _ in range(W):
+            stack.copy_in()
+            stack.step()
+            stack.copy_out()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stack.stream)
+        for _ in range(K):
+            stack.copy_in()
+            stack.step()
+            stack.copy_out()
+        e1.record(stack.stream)
+        torch.cuda.synchronize()
+        barrier()
+    return e0.elapsed_time(e1)
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_decode_sample(inp, budget_s: float):
+    """Times the fp64 oracle's decode step on `inp` until budget_s passes
+    (at least one step). Returns (state GB/s, steps, seconds)."""
+    import oracle
+    M = inp["M"]
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_step(inp["x_f32"][0], inp["conv_w"], inp["cache_f32"], inp["alpha"][0],
+                           inp["beta"][0], inp["S0"])
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return state_bytes_per_launch(M, "f32") * steps / el / 1e9, steps, el
+
+
+def config_dict(M, state_dtype, x_dtype, layers=LAYERS):
+    return {
+        "workload": "KDA decode step, %d-layer stack, M=%d streams x %d heads x %dx%d %s "
+                    "state, fused conv+SiLU+L2norm, %s q/k/v and conv cache"
+                    % (layers, M, H, DH, DH, state_dtype.upper(), x_dtype.upper()),
+        "M": M, "H": H, "dk": DH, "dv": DH, "layers": layers,
+        "state_dtype": state_dtype, "x_dtype": x_dtype,
+        "l2": "inputs larger than L2: each step touches %d layers x %.0f MB of state, "
+              "visited in turn" % (layers, state_bytes_per_launch(M, state_dtype) / 2e6),
+    }
+
+
+# --------------------------------------------------------------------------- arms
+def reference_arm(args, rank: int):
+    """The fp64 CPU oracle on this host's cores, on a bounded sample of the
+    same workload per step (one stream of one layer)."""
+    if rank != 0:
+        return
+    from linear_attention_decode_step_gb300 import inputs
+    samples = [inputs.decode_layer(inputs.layer_seed(3, l), M=1, T=1) for l in range(4)]
+    import oracle
+    oracle.build()
+    for i in range(args.warmup):
+        oracle_decode_sample(samples[i % 4], 0.0)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_decode_sample(samples[i % 4], 0.0)
+    el = time.perf_counter() - t0
+    per_step_bytes = state_bytes_per_launch(1, "f32")
+    value = per_step_bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(args.M, "f32", "bf16"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "per step: one decode step of one layer for one stream "
+                                   "(64 heads, 128x128 state), fp64 C oracle, single thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def own_arm(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    from linear_attention_decode_step_gb300 import build, inputs, kda
+
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    stack = DecodeStack(torch, kda, inputs, args.M, args.layers, args.state_dtype, args.x_dtype,
+                        dev)
+    clocks = ClockSampler(gpu_uuid(torch, dev))
+    clocks.start()
+    total_ms, launch_ms = time_device(stack, args.steps, args.warmup, barrier)
+    clk = clocks.stop()
+    e2e_ms = time_e2e(stack, args.steps, max(3, args.warmup // 4), barrier)
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    K = args.steps
+    sb = state_bytes_per_launch(args.M, args.state_dtype)
+    ab = algorithmic_bytes_per_launch(args.M, args.state_dtype, args.x_dtype)
+    L = args.layers
+    value = world * L * K * sb / (total_ms * 1e-3) / 1e9
+    e2e_value = world * L * K * sb / (e2e_ms * 1e-3) / 1e9
+    mean_launch_ms = float(np.mean(launch_ms))
+    peak, peak_kind = measured_peak()
+    achieved = ab / (mean_launch_ms * 1e-3) / 1e9
+    traffic = ncu_traffic_per_launch() if (args.M == 32 and args.state_dtype == "f32") else None
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if args.state_dtype == "f32" else "f32 (bf16 state storage)",
+        "data": "synthetic", "config": config_dict(args.M, args.state_dtype, args.x_dtype),
+        "ms_per_layer": total_ms / K / L,
+        "state_gbs_frac_of_%s_hbm" % peak_kind: value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "kda_decode_kernel", "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": ab,
+                     "mean_launch_us": mean_launch_ms * 1e3},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": stack.h2d_bytes(),
+                "d2h_bytes_per_step": stack.d2h_bytes()},
+        "gpu_launches": K * L,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, n, el = oracle_decode_sample(stack.host0, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "layer 0 of the workload (M=%d, 64 heads) decoded %d times by the "
+                      "fp64 C oracle, single thread, %.1f s" % (args.M, n, el)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["own", "reference"], default="own")
+    ap.add_argument("--M", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers in the stack (34 in GLM-5.3-Flash; fewer only for profiling)")
+    ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--x-dtype", choices=["f32", "bf16"], default="bf16")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        own_arm(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

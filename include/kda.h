@@ -1,0 +1,133 @@
+/*
+ * kda.h — C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * What it computes. Per stream m and head h, one decode step of a KDA layer:
+ *   1. short convolution, kernel 4 (three cached taps), followed by SiLU, on
+ *      each channel of the pre-conv q, k and v
+ *      ("GLM-5.3 deep dive", section 8.2.4, steps 2 and 6; channel layout
+ *      from "At the 262k cap the DSA indexer costs 12x the sparse MLA it
+ *      selects for", section "Geometry": depthwise, weight [8192, 1, 4]);
+ *   2. L2 normalisation of q and k: x / sqrt(sum x^2 + 1e-6)
+ *      ("GLM-5.3 deep dive", section 8.2.6, implementation notes);
+ *   3. the gated delta rule ("GLM-5.3 deep dive", section 8.2.3, Eq. 1)
+ *         S <- (I - beta k k^T) Diag(alpha) S + beta k v^T,
+ *      taken in the four-step order of section 8.2.6 (fade, predict,
+ *      correct), on a dk x dv state;
+ *   4. the readout o = scale * S^T q from the updated state (Eq. 1 with
+ *      scale = 1; fla's default is 1 / sqrt(dk)).
+ * The chunked prefill computes the same recurrence over T tokens of
+ * post-conv q, k, v in the chunkwise WY / UT form of section 8.2.5 (Eq. 6-9).
+ *
+ * Conventions shared by every entry point.
+ *   - Every buffer argument is a DEVICE pointer, owned by the caller. The
+ *     library allocates nothing and keeps no pointer after the call returns.
+ *   - Arrays are dense, row-major (C order), with the layouts stated per
+ *     argument. D = H * d is the number of channels of one of q, k, v.
+ *   - Every buffer pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued on it; calls return without waiting.
+ *   - Arguments are checked on the host before anything is launched. On any
+ *     error status other than KDA_ERR_CUDA no buffer has been touched.
+ *   - KDA_ERR_CUDA means a CUDA runtime call failed (for example the launch);
+ *     kda_last_cuda_error() gives the cudaError_t value, per host thread.
+ *   - No exceptions cross this boundary. There is no CPU fallback: every step
+ *     of the computation runs in this library's kernels.
+ *   - The entry points are thread-safe; they keep no mutable global state
+ *     other than the per-thread last CUDA error.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, overlapping outputs */
+    KDA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. dk != 128) */
+    KDA_ERR_ALIGNMENT = 3,   /* a buffer pointer is not 16-byte aligned */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call failed; see kda_last_cuda_error() */
+    KDA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum {
+    KDA_F32 = 0,  /* IEEE binary32 */
+    KDA_BF16 = 1  /* bfloat16; values are widened exactly, stores round to nearest even */
+} kda_dtype;
+
+/* Human-readable name of a status code. Never NULL; static storage. */
+const char *kda_status_string(int status);
+
+/* cudaError_t of the last failed CUDA call made by this host thread inside
+ * the library (0 if none). */
+int kda_last_cuda_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int kda_version(void);
+
+/*
+ * kda_conv_step — short convolution + SiLU for one token, q, k and v at once.
+ * ("GLM-5.3 deep dive", section 8.2.4, step 2; kernel 4, no bias.)
+ *
+ *   x           [M, 3, D]    pre-conv q, k, v of this token (x_dtype)
+ *   conv_w      [3, D, 4]    FP32 weights; [.][c][3] multiplies the current
+ *                            token, [.][c][0] the oldest cached one
+ *   conv_cache  [M, 3, 3, D] the three previous inputs per channel, tap 0
+ *                            oldest (cache_dtype, must equal x_dtype).
+ *                            Updated in place to (tap1, tap2, x).
+ *   y           [M, 3, D]    FP32 output: SiLU(w . [cache, x])
+ *   M >= 1 streams, D >= 1 channels per tensor.
+ * y must not overlap x, conv_w or conv_cache.
+ */
+kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w,
+                         void *conv_cache, int cache_dtype, float *y,
+                         int M, int D, void *stream);
+
+/*
+ * kda_decode_step — one fused KDA decode step for M streams (conv + SiLU,
+ * L2 norm of q and k, Eq. 1 update, readout), one launch.
+ *
+ *   x           [M, 3, H*dk] pre-conv q, k, v of this token (x_dtype)
+ *   conv_w      [3, H*dk, 4] FP32 conv weights (as in kda_conv_step)
+ *   conv_cache  [M, 3, 3, H*dk] conv cache (cache_dtype == x_dtype), in place
+ *   alpha       [M, H, dk]   FP32 per-key-channel decay, linear space (0, 1]
+ *   beta        [M, H]       FP32 write strength per head
+ *   state       [M, H, dk, dv] recurrent state S[i][j] (i: key channel,
+ *                            j: value channel), state_dtype; read and
+ *                            written in place. With BF16 storage the
+ *                            arithmetic is FP32 and the readout uses the
+ *                            unrounded updated state; only the store rounds.
+ *   scale       multiplies the readout (1.0 reproduces Eq. 1)
+ *   o           [M, H, dv]   FP32 output
+ *   dk = dv = 128 (other sizes return KDA_ERR_UNSUPPORTED); 1 <= M, H <= 65535.
+ * o must not overlap state, conv_cache or x; state must not overlap conv_cache.
+ */
+kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w,
+                           void *conv_cache, int cache_dtype,
+                           const float *alpha, const float *beta,
+                           void *state, int state_dtype, float scale,
+                           float *o, int M, int H, int dk, int dv, void *stream);
+
+/*
+ * kda_decode_step_tile — kda_decode_step with an explicit work split, for
+ * tuning and tests. Each head's dv value columns are split into slices of
+ * `columns` (16, 32, 64 or 128), one CTA of `threads` threads each; the
+ * slices of one head form a thread-block cluster. kda_decode_step picks the
+ * split itself. Unsupported (columns, threads) pairs return
+ * KDA_ERR_UNSUPPORTED.
+ */
+kda_status kda_decode_step_tile(const void *x, int x_dtype, const float *conv_w,
+                                void *conv_cache, int cache_dtype,
+                                const float *alpha, const float *beta,
+                                void *state, int state_dtype, float scale,
+                                float *o, int M, int H, int dk, int dv,
+                                int columns, int threads, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

@@ -1,0 +1,134 @@
+// C ABI of the KDA library (declared and documented in include/kda.h):
+// host-side argument checks, then one kernel launch on the caller's stream.
+// Nothing here allocates memory or synchronises the device.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+kda_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return KDA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(int t) { return t == KDA_F32 || t == KDA_BF16; }
+
+size_t dtype_bytes(int t) { return t == KDA_BF16 ? 2u : 4u; }
+
+// [a, a + na) and [b, b + nb) overlap
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
+                        int cache_dtype, const float *alpha, const float *beta, void *state,
+                        int state_dtype, float *o, int M, int H, int dk, int dv) {
+    if (!x || !conv_w || !conv_cache || !alpha || !beta || !state || !o)
+        return KDA_ERR_INVALID_ARG;
+    if (M <= 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(x_dtype) || !valid_dtype(cache_dtype) || !valid_dtype(state_dtype))
+        return KDA_ERR_INVALID_ARG;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (cache_dtype != x_dtype) return KDA_ERR_UNSUPPORTED;
+    if (M > 65535 || H > 65535) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_cache) || !aligned16(alpha) ||
+        !aligned16(beta) || !aligned16(state) || !aligned16(o))
+        return KDA_ERR_ALIGNMENT;
+    const size_t D = (size_t)H * dk;
+    const size_t n_state = (size_t)M * H * dk * dv * dtype_bytes(state_dtype);
+    const size_t n_o = (size_t)M * H * dv * sizeof(float);
+    const size_t n_cache = (size_t)M * 9 * D * dtype_bytes(cache_dtype);
+    const size_t n_x = (size_t)M * 3 * D * dtype_bytes(x_dtype);
+    if (overlap(o, n_o, state, n_state) || overlap(o, n_o, conv_cache, n_cache) ||
+        overlap(o, n_o, x, n_x) || overlap(state, n_state, conv_cache, n_cache))
+        return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_ALIGNMENT: return "KDA_ERR_ALIGNMENT";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kda_version(void) { return 100; }
+
+kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
+                         int cache_dtype, float *y, int M, int D, void *stream) {
+    if (!x || !conv_w || !conv_cache || !y) return KDA_ERR_INVALID_ARG;
+    if (M <= 0 || D <= 0) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(x_dtype) || !valid_dtype(cache_dtype)) return KDA_ERR_INVALID_ARG;
+    if (cache_dtype != x_dtype) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_cache) || !aligned16(y))
+        return KDA_ERR_ALIGNMENT;
+    const size_t n_y = (size_t)M * 3 * D * sizeof(float);
+    const size_t b = dtype_bytes(x_dtype);
+    if (overlap(y, n_y, x, (size_t)M * 3 * D * b) ||
+        overlap(y, n_y, conv_cache, (size_t)M * 9 * D * b) ||
+        overlap(y, n_y, conv_w, (size_t)3 * D * 4 * sizeof(float)))
+        return KDA_ERR_INVALID_ARG;
+    return cuda_status(kda::launch_conv(x, x_dtype, conv_w, conv_cache, y, M, D,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_decode_step_tile(const void *x, int x_dtype, const float *conv_w,
+                                void *conv_cache, int cache_dtype, const float *alpha,
+                                const float *beta, void *state, int state_dtype, float scale,
+                                float *o, int M, int H, int dk, int dv, int columns, int threads,
+                                void *stream) {
+    const kda_status st = check_decode(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta,
+                                       state, state_dtype, o, M, H, dk, dv);
+    if (st != KDA_OK) return st;
+    kda::DecodeArgs a;
+    a.x = x;
+    a.conv_w = conv_w;
+    a.cache = conv_cache;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.state = state;
+    a.o = o;
+    a.M = M;
+    a.H = H;
+    a.scale = scale;
+    const cudaError_t e = kda::launch_decode(a, x_dtype, state_dtype, columns, threads,
+                                             static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
+                           int cache_dtype, const float *alpha, const float *beta, void *state,
+                           int state_dtype, float scale, float *o, int M, int H, int dk, int dv,
+                           void *stream) {
+    int columns = 0, threads = 0;
+    kda::default_decode_tile(M, H, state_dtype, &columns, &threads);
+    return kda_decode_step_tile(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta, state,
+                                state_dtype, scale, o, M, H, dk, dv, columns, threads, stream);
+}
+
+}  // extern "C"

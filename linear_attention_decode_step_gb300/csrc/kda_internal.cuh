@@ -1,0 +1,39 @@
+// Internal declarations shared by the library's translation units (not part
+// of the public ABI; the public surface is include/kda.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kda {
+
+constexpr int kHeadDim = 128;  // dk = dv handled by the decode and prefill kernels
+
+// Arguments of one fused decode step (layouts as documented in kda.h).
+struct DecodeArgs {
+    const void *x;         // [M, 3, H*128] pre-conv q, k, v
+    const float *conv_w;   // [3, H*128, 4]
+    void *cache;           // [M, 3, 3, H*128]
+    const float *alpha;    // [M, H, 128]
+    const float *beta;     // [M, H]
+    void *state;           // [M, H, 128, 128]
+    float *o;              // [M, H, 128]
+    int M, H;
+    float scale;
+};
+
+// Launches the decode kernel for the given storage types and work split.
+// Returns cudaErrorNotSupported (without launching) when no kernel is
+// instantiated for (columns, threads).
+cudaError_t launch_decode(const DecodeArgs &a, int x_dtype, int state_dtype,
+                          int columns, int threads, cudaStream_t stream);
+
+// Picks the decode work split (columns per CTA, threads per CTA) for M.
+void default_decode_tile(int M, int H, int state_dtype, int *columns, int *threads);
+
+// Standalone short conv + SiLU for one token.
+cudaError_t launch_conv(const void *x, int x_dtype, const float *conv_w, void *cache,
+                        float *y, int M, int D, cudaStream_t stream);
+
+}  // namespace kda

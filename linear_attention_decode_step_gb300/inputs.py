@@ -17,6 +17,9 @@ pages (64 heads x 128 x 128 state, kernel-4 short convolution):
 * initial state S0 ~ N(0, 0.1^2), rounded to BF16 and widened to FP32, so that
   FP32 and BF16 state storage start from identical values.
 
+Large normal arrays are drawn directly in float32 (numpy's float32 path);
+the small per-head beta and alpha draws are float64 then stored as FP32.
+
 Draw order for a decode layer: conv_w, conv cache, S0, then per step
 (x, beta_raw, alpha_raw).  Draw order for a prefill problem: S0, q, k, v,
 beta_raw, alpha_raw.  The generator is numpy's PCG64 (``default_rng``).
@@ -40,8 +43,12 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     Inputs here are finite normal draws, so no NaN handling is needed.
     """
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    lsb = (b >> np.uint32(16)) & np.uint32(1)
-    return ((b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    r = b >> np.uint32(16)
+    r &= np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += b
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_widen(bits: np.ndarray) -> np.ndarray:
@@ -75,12 +82,15 @@ def decode_layer(seed: int, M: int, H: int = 64, d: int = 128, T: int = 1,
     """
     rng = np.random.default_rng(seed)
     D = H * d
-    conv_w = (rng.standard_normal((3, D, 4)) * 0.5).astype(np.float32)
-    cache_bits = bf16_bits(rng.standard_normal((M, 3, 3, D)).astype(np.float32))
-    S0 = bf16_widen(bf16_bits((rng.standard_normal((M, H, d, d)) * 0.1).astype(np.float32)))
+    conv_w = rng.standard_normal((3, D, 4), dtype=np.float32)
+    conv_w *= np.float32(0.5)
+    cache_bits = bf16_bits(rng.standard_normal((M, 3, 3, D), dtype=np.float32))
+    S0 = rng.standard_normal((M, H, d, d), dtype=np.float32)
+    S0 *= np.float32(0.1)
+    S0 = bf16_widen(bf16_bits(S0))
     x_bits, beta, alpha = [], [], []
     for _ in range(T):
-        x_bits.append(bf16_bits(rng.standard_normal((M, 3, D)).astype(np.float32)))
+        x_bits.append(bf16_bits(rng.standard_normal((M, 3, D), dtype=np.float32)))
         beta.append(_sigmoid32(rng.standard_normal((M, H))))
         alpha.append(_sigmoid32(rng.standard_normal((M, H, d)) + alpha_mean))
     return {
@@ -105,7 +115,9 @@ def prefill_problem(seed: int, M: int, T: int, H: int = 64, d: int = 128,
     and S0 float32 [M, H, d, d] (BF16-representable values).
     """
     rng = np.random.default_rng(seed)
-    S0 = bf16_widen(bf16_bits((rng.standard_normal((M, H, d, d)) * 0.1).astype(np.float32)))
+    S0 = rng.standard_normal((M, H, d, d), dtype=np.float32)
+    S0 *= np.float32(0.1)
+    S0 = bf16_widen(bf16_bits(S0))
     out = {"M": M, "T": T, "H": H, "d": d, "S0": np.ascontiguousarray(S0)}
     for name in ("q", "k", "v"):
         bits = bf16_bits(rng.standard_normal((M, T, H, d), dtype=np.float32))

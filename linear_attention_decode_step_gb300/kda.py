@@ -1,0 +1,184 @@
+"""Python binding of the KDA C ABI (include/kda.h), via ctypes.
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream to libkda_gb300.so and raises ``KdaError`` on a
+non-OK status. Nothing here computes any part of the method, and there is no
+fallback: if the library is missing, loading fails loudly.
+
+Names mirror the C entry points (``kda_conv_step``, ``kda_decode_step``,
+``kda_chunk_prefill``...). Tensors are torch CUDA tensors, contiguous, in the
+layouts documented in kda.h; PyTorch is used only for device memory and
+streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+__all__ = [
+    "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_ALIGNMENT",
+    "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_F32", "KDA_BF16",
+    "KdaError", "lib", "library_path", "header_functions",
+    "kda_status_string", "kda_last_cuda_error", "kda_version",
+    "kda_conv_step", "kda_decode_step", "kda_decode_step_tile",
+]
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
+KDA_ERR_ALIGNMENT, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
+KDA_F32, KDA_BF16 = 0, 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_HEADER = os.path.join(os.path.dirname(_PKG), "include", "kda.h")
+_lock = threading.Lock()
+_lib = None
+
+_V, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+# C signatures (argument types, return type) of every exported entry point
+_SIGNATURES = {
+    "kda_status_string": ([_I], ctypes.c_char_p),
+    "kda_last_cuda_error": ([], _I),
+    "kda_version": ([], _I),
+    "kda_conv_step": ([_V, _I, _V, _V, _I, _V, _I, _I, _V], _I),
+    "kda_decode_step": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
+                         _I, _I, _I, _I, _V], _I),
+    "kda_decode_step_tile": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
+                              _I, _I, _I, _I, _I, _I, _V], _I),
+}
+
+
+class KdaError(RuntimeError):
+    """A KDA entry point returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = "%s failed: %s" % (fn, _status_name(status))
+        if status == KDA_ERR_CUDA:
+            msg += " (cudaError %d)" % lib().kda_last_cuda_error()
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libkda_gb300.so")
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/kda.h."""
+    text = open(_HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "libkda_gb300.so is not built (expected at %s); run "
+                    "linear_attention_decode_step_gb300.build.build()" % path)
+            L = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                f = getattr(L, name)
+                f.argtypes, f.restype = args, res
+            _lib = L
+    return _lib
+
+
+def _status_name(status: int) -> str:
+    return lib().kda_status_string(status).decode()
+
+
+def kda_status_string(status: int) -> str:
+    return _status_name(status)
+
+
+def kda_last_cuda_error() -> int:
+    return lib().kda_last_cuda_error()
+
+
+def kda_version() -> int:
+    return lib().kda_version()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KDA_OK:
+        raise KdaError(fn, status)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def kda_conv_step(x, conv_w, conv_cache, y=None, stream=None):
+    """Short conv + SiLU for one token. x [M,3,D] (bf16|f32), conv_w [3,D,4]
+    f32, conv_cache [M,3,3,D] (same dtype as x, updated in place) -> y
+    [M,3,D] f32."""
+    M, three, D = x.shape
+    if y is None:
+        y = torch.empty((M, 3, D), dtype=torch.float32, device=x.device)
+    st = lib().kda_conv_step(_dev(x, "x"), _dtype_code(x), _dev(conv_w, "conv_w", torch.float32),
+                             _dev(conv_cache, "conv_cache"), _dtype_code(conv_cache),
+                             _dev(y, "y", torch.float32), M, D, _stream(stream))
+    _check("kda_conv_step", st)
+    return y
+
+
+def _decode_args(x, conv_w, conv_cache, alpha, beta, state, o):
+    M, H, dk, dv = state.shape
+    if o is None:
+        o = torch.empty((M, H, dv), dtype=torch.float32, device=state.device)
+    args = [_dev(x, "x"), _dtype_code(x), _dev(conv_w, "conv_w", torch.float32),
+            _dev(conv_cache, "conv_cache"), _dtype_code(conv_cache),
+            _dev(alpha, "alpha", torch.float32), _dev(beta, "beta", torch.float32),
+            _dev(state, "state"), _dtype_code(state)]
+    return M, H, dk, dv, o, args
+
+
+def kda_decode_step(x, conv_w, conv_cache, alpha, beta, state, o=None, scale=1.0,
+                    stream=None):
+    """One fused KDA decode step (see kda.h). state [M,H,128,128] (f32|bf16)
+    and conv_cache are updated in place; returns o [M,H,128] f32."""
+    M, H, dk, dv, o, args = _decode_args(x, conv_w, conv_cache, alpha, beta, state, o)
+    st = lib().kda_decode_step(*args, float(scale), _dev(o, "o", torch.float32),
+                               M, H, dk, dv, _stream(stream))
+    _check("kda_decode_step", st)
+    return o
+
+
+def kda_decode_step_tile(x, conv_w, conv_cache, alpha, beta, state, o=None, scale=1.0,
+                         columns=32, threads=128, stream=None):
+    """kda_decode_step with an explicit (columns per CTA, threads per CTA)."""
+    M, H, dk, dv, o, args = _decode_args(x, conv_w, conv_cache, alpha, beta, state, o)
+    st = lib().kda_decode_step_tile(*args, float(scale), _dev(o, "o", torch.float32),
+                                    M, H, dk, dv, int(columns), int(threads), _stream(stream))
+    _check("kda_decode_step_tile", st)
+    return o

@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads, exports every symbol include/kda.h
+declares, and rejects bad arguments on the host before touching the device.
+
+These run without a GPU: every call below returns from the host-side checks
+(fake but aligned, non-overlapping addresses are never dereferenced).
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from linear_attention_decode_step_gb300 import build as kbuild
+
+
+@pytest.fixture(scope="module")
+def K():
+    kbuild.build()
+    from linear_attention_decode_step_gb300 import kda
+    return kda
+
+
+def test_header_symbols_exported(K):
+    names = K.header_functions()
+    assert {"kda_conv_step", "kda_decode_step", "kda_status_string"} <= set(names)
+    L = K.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", K.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert set(names) <= exported
+    # every declared function has a binding signature
+    assert set(names) <= set(K._SIGNATURES)
+
+
+def test_status_strings(K):
+    assert K.kda_status_string(0) == "KDA_OK"
+    assert K.kda_status_string(4) == "KDA_ERR_CUDA"
+    assert K.kda_status_string(99) == "KDA_ERR_UNKNOWN"
+    assert K.kda_version() >= 100
+    assert K.kda_last_cuda_error() == 0
+
+
+# fake device addresses: 16-byte aligned, far apart (never dereferenced)
+BASE = 1 << 40
+GAP = 1 << 34
+
+
+def _decode_call(K, **over):
+    a = dict(x=BASE, xd=K.KDA_BF16, w=BASE + GAP, cache=BASE + 2 * GAP, cd=K.KDA_BF16,
+             alpha=BASE + 3 * GAP, beta=BASE + 4 * GAP, state=BASE + 5 * GAP,
+             sd=K.KDA_F32, scale=1.0, o=BASE + 6 * GAP, M=4, H=64, dk=128, dv=128)
+    a.update(over)
+    return K.lib().kda_decode_step(a["x"], a["xd"], a["w"], a["cache"], a["cd"], a["alpha"],
+                                   a["beta"], a["state"], a["sd"], a["scale"], a["o"],
+                                   a["M"], a["H"], a["dk"], a["dv"], None)
+
+
+@pytest.mark.parametrize("field", ["x", "w", "cache", "alpha", "beta", "state", "o"])
+def test_decode_null_pointer(K, field):
+    assert _decode_call(K, **{field: None}) == K.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field", ["x", "w", "cache", "alpha", "beta", "state", "o"])
+def test_decode_misaligned(K, field):
+    base = {"x": BASE, "w": BASE + GAP, "cache": BASE + 2 * GAP, "alpha": BASE + 3 * GAP,
+            "beta": BASE + 4 * GAP, "state": BASE + 5 * GAP, "o": BASE + 6 * GAP}[field]
+    assert _decode_call(K, **{field: base + 4}) == K.KDA_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(M=0), 1), (dict(H=0), 1), (dict(M=-3), 1), (dict(dk=0), 1),
+    (dict(dk=64), 2), (dict(dv=64), 2), (dict(dk=256, dv=256), 2),
+    (dict(M=70000), 2), (dict(xd=7), 1), (dict(sd=-1), 1), (dict(cd=5), 1),
+    (dict(cd=0), 2),                       # cache dtype must equal x dtype
+    (dict(o=BASE + 5 * GAP + 1024), 1),    # o inside the state buffer
+    (dict(cache=BASE + 5 * GAP), 1),       # cache aliases the state
+])
+def test_decode_rejects(K, over, status):
+    assert _decode_call(K, **over) == status
+
+
+def test_decode_unsupported_tile(K):
+    L = K.lib()
+    st = L.kda_decode_step_tile(BASE, 1, BASE + GAP, BASE + 2 * GAP, 1, BASE + 3 * GAP,
+                                BASE + 4 * GAP, BASE + 5 * GAP, 0, 1.0, BASE + 6 * GAP,
+                                4, 64, 128, 128, 48, 96, None)
+    assert st == K.KDA_ERR_UNSUPPORTED
+
+
+def test_conv_rejects(K):
+    L = K.lib()
+    ok = dict(x=BASE, xd=1, w=BASE + GAP, c=BASE + 2 * GAP, cd=1, y=BASE + 3 * GAP, M=2, D=8192)
+
+    def call(**o):
+        a = dict(ok)
+        a.update(o)
+        return L.kda_conv_step(a["x"], a["xd"], a["w"], a["c"], a["cd"], a["y"],
+                               a["M"], a["D"], None)
+    assert call(x=None) == K.KDA_ERR_INVALID_ARG
+    assert call(y=BASE + 3 * GAP + 2) == K.KDA_ERR_ALIGNMENT
+    assert call(M=0) == K.KDA_ERR_INVALID_ARG
+    assert call(cd=0) == K.KDA_ERR_UNSUPPORTED
+    assert call(y=BASE + 16) == K.KDA_ERR_INVALID_ARG   # y overlaps x
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from linear_attention_decode_step_gb300 import kda
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(kda, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        kda.lib()

@@ -1,0 +1,201 @@
+"""GPU parity of the fused decode step against the fp64 oracle.
+
+Every comparison is element by element on the same seeded inputs:
+max |gpu - oracle| / max |oracle| <= 1e-4 with FP32 state storage and
+<= 5e-3 with BF16 state storage, on o and on S separately; the conv cache is
+a pure copy and must match exactly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from linear_attention_decode_step_gb300 import inputs
+from tests.kda_testlib import (TOL_BF16_STATE, TOL_F32_STATE, DeviceLayer, oracle_layer,
+                               rel_err, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from linear_attention_decode_step_gb300 import build
+    build.build()
+    from linear_attention_decode_step_gb300 import kda
+    return kda
+
+
+def _tol(state_dtype):
+    return TOL_BF16_STATE if state_dtype == "bf16" else TOL_F32_STATE
+
+
+def _run(K, dl: DeviceLayer, steps, scale=1.0, tile=None, graph=False):
+    outs = []
+    for t in range(steps):
+        if tile is None:
+            K.kda_decode_step(dl.x[t], dl.conv_w, dl.cache, dl.alpha[t], dl.beta[t], dl.state,
+                              dl.o, scale=scale)
+        else:
+            K.kda_decode_step_tile(dl.x[t], dl.conv_w, dl.cache, dl.alpha[t], dl.beta[t],
+                                   dl.state, dl.o, scale=scale, columns=tile[0], threads=tile[1])
+        outs.append(dl.o.double().cpu().numpy())
+    torch.cuda.synchronize()
+    return outs
+
+
+def _compare(dl, outs, ref_outs, S_ref, cache_ref, tol):
+    for t, (o, r) in enumerate(zip(outs, ref_outs)):
+        e = rel_err(o, r)
+        assert e <= tol, "o at step %d: rel err %.3e > %.1e" % (t, e, tol)
+    e = rel_err(to_f64(dl.state), S_ref)
+    assert e <= tol, "S: rel err %.3e > %.1e" % (e, tol)
+    np.testing.assert_array_equal(to_f64(dl.cache), cache_ref)
+
+
+def test_config0_fp32_sixteen_steps(K):
+    """M=1, H=64, 128x128, FP32 state, 16 consecutive steps from seed."""
+    inp = inputs.decode_layer(inputs.layer_seed(0, 0), M=1, T=16)
+    dl = DeviceLayer(inp, "f32")
+    outs = _run(K, dl, 16)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
+
+
+def test_config1_fp32_M8(K):
+    inp = inputs.decode_layer(inputs.layer_seed(1, 0), M=8, T=1)
+    dl = DeviceLayer(inp, "f32")
+    outs = _run(K, dl, 1)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
+
+
+def test_config2_bf16_M32(K):
+    """M=32, BF16 state storage, FP32 arithmetic; S0 identical to the FP32 run."""
+    inp = inputs.decode_layer(inputs.layer_seed(2, 0), M=32, T=1)
+    dl = DeviceLayer(inp, "bf16")
+    outs = _run(K, dl, 1)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_BF16_STATE)
+    # one BF16 rounding of the updated state: within half an ulp of the exact
+    # value. BF16 keeps 8 significant bits (7 stored), so half an ulp is at
+    # most 2^-8 of the value's magnitude; plus FP32 arithmetic noise.
+    got = to_f64(dl.state)
+    assert np.all(np.abs(got - S) <= 2.0 ** -8 * np.abs(S) + 1e-6 * np.max(np.abs(S)))
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_M32_one_step(K, state_dtype):
+    """The benchmarked workload: M=32, one step, fused conv."""
+    inp = inputs.decode_layer(inputs.layer_seed(3, 32), M=32, T=1)
+    dl = DeviceLayer(inp, state_dtype)
+    outs = _run(K, dl, 1)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, _tol(state_dtype))
+
+
+TILES = [(16, 64), (32, 64), (32, 128), (64, 128), (64, 256), (128, 256)]
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+def test_every_tile(K, tile, state_dtype, x_dtype):
+    inp = inputs.decode_layer(77, M=3, H=5, T=3)
+    dl = DeviceLayer(inp, state_dtype, x_dtype)
+    outs = _run(K, dl, 3, tile=tile)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, _tol(state_dtype))
+
+
+def test_odd_sizes_and_scale(K):
+    inp = inputs.decode_layer(5, M=5, H=3, T=4)
+    dl = DeviceLayer(inp, "f32")
+    scale = 128 ** -0.5
+    outs = _run(K, dl, 4, scale=scale)
+    ref, S, cache = oracle_layer(inp, scale=scale)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
+
+
+def test_max_streams_M64(K):
+    inp = inputs.decode_layer(inputs.layer_seed(3, 64), M=64, T=1)
+    dl = DeviceLayer(inp, "f32")
+    outs = _run(K, dl, 1)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_identity_step_leaves_state(K, state_dtype):
+    """alpha = 1, beta = 0: the state is returned bit for bit and o = S^T q."""
+    inp = inputs.decode_layer(6, M=2, H=4, T=1)
+    inp["alpha"] = [np.ones_like(inp["alpha"][0])]
+    inp["beta"] = [np.zeros_like(inp["beta"][0])]
+    dl = DeviceLayer(inp, state_dtype)
+    before = dl.state.clone()
+    outs = _run(K, dl, 1)
+    assert torch.equal(before, dl.state)
+    ref, S, cache = oracle_layer(inp)
+    assert rel_err(outs[0], ref[0]) <= TOL_F32_STATE
+
+
+def test_exact_write_beta_one(K):
+    """beta = 1: after the step, reading with the normalised key returns v
+    (section 8.2.3), checked against the oracle's state."""
+    inp = inputs.decode_layer(8, M=2, H=4, T=1)
+    inp["beta"] = [np.ones_like(inp["beta"][0])]
+    dl = DeviceLayer(inp, "f32")
+    outs = _run(K, dl, 1)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
+
+
+def test_zero_input_degenerate(K):
+    """All-zero pre-conv input and cache: q = k = 0 after the conv, so the
+    update only fades the state and o = 0."""
+    inp = inputs.decode_layer(9, M=2, H=4, T=1)
+    inp["x_bits"] = [np.zeros_like(inp["x_bits"][0])]
+    inp["x_f32"] = [np.zeros_like(inp["x_f32"][0])]
+    inp["cache_bits"] = np.zeros_like(inp["cache_bits"])
+    inp["cache_f32"] = np.zeros_like(inp["cache_f32"])
+    dl = DeviceLayer(inp, "f32")
+    outs = _run(K, dl, 1)
+    ref, S, cache = oracle_layer(inp)
+    assert np.all(outs[0] == 0.0)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_34_layer_stack_under_cuda_graph(K, state_dtype):
+    """34 independent layers, M=8, one token, launched as one captured CUDA
+    graph (the bench's launch configuration); every layer checked."""
+    L, M = 34, 8
+    layers = [DeviceLayer(inputs.decode_layer(inputs.layer_seed(3, l), M=M, T=1), state_dtype)
+              for l in range(L)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for dl in layers:
+                K.kda_decode_step(dl.x[0], dl.conv_w, dl.cache, dl.alpha[0], dl.beta[0],
+                                  dl.state, dl.o)
+    g.replay()
+    torch.cuda.synchronize()
+    for dl in layers:
+        ref, S, cache = oracle_layer(dl.inp)
+        _compare(dl, [dl.o.double().cpu().numpy()], ref, S, cache, _tol(state_dtype))
+
+
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+def test_conv_step(K, x_dtype):
+    inp = inputs.decode_layer(10, M=3, H=64, T=2)
+    dl = DeviceLayer(inp, "f32", x_dtype)
+    cache = inp["cache_f32"].astype(np.float64)
+    for t in range(2):
+        y = K.kda_conv_step(dl.x[t], dl.conv_w, dl.cache)
+        y_ref, cache = oracle.conv_step(inp["x_f32"][t], inp["conv_w"], cache)
+        torch.cuda.synchronize()
+        assert rel_err(y.double().cpu().numpy(), y_ref) <= 1e-6
+        np.testing.assert_array_equal(to_f64(dl.cache), cache)
