@@ -40,7 +40,10 @@ UNIT = "GB/s"
 H, DH = 64, 128
 LAYERS = 34
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "linear_attention_decode_step_gb300", "csrc", "kda_decode.cu")
+CSRC = os.path.join(ROOT, "linear_attention_decode_step_gb300", "csrc")
+# the kernel kda_decode_step runs for this workload (M*H >= 512 heads) and its source
+DECODE_KERNEL = "kda_decode_stream_kernel"
+DECODE_SRC = os.path.join(CSRC, "kda_decode_stream.cu")
 TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_decode_M32_f32.md")
 
 
@@ -158,7 +161,10 @@ class DecodeStack:
     """L independent KDA layers resident on one GPU, with pinned host
     mirrors of the per-step inputs and outputs for the end-to-end leg."""
 
-    def __init__(self, torch, kda, inputs, M, L, state_dtype, x_dtype, device, seed_cfg=3):
+    def __init__(self, torch, kda, inputs, M, L, state_dtype, x_dtype, device, seed_cfg=3,
+                 kernel=0, columns=0, threads=0, replicate=False):
+        """replicate=True draws one layer's inputs and copies them into every
+        layer's buffers (used by the sweep, where only timing matters)."""
         self.torch, self.kda, self.M, self.L = torch, kda, M, L
         self.state_dtype, self.x_dtype = state_dtype, x_dtype
         D = H * DH
@@ -172,7 +178,8 @@ class DecodeStack:
         self.conv_w, self.cache, self.state = [], [], []
         self.host0 = None
         for l in range(L):
-            inp = inputs.decode_layer(inputs.layer_seed(seed_cfg, l), M=M, T=1)
+            if l == 0 or not replicate:
+                inp = inputs.decode_layer(inputs.layer_seed(seed_cfg, l), M=M, T=1)
             if l == 0:
                 self.host0 = inp
             if x_dtype == "bf16":
@@ -195,14 +202,21 @@ class DecodeStack:
         sp = self.stream.cuda_stream
         xd = kda.KDA_BF16 if x_dtype == "bf16" else kda.KDA_F32
         sd = kda.KDA_BF16 if state_dtype == "bf16" else kda.KDA_F32
-        # marshalled C-ABI arguments of each layer's kda_decode_step call
+        # marshalled C-ABI arguments of each layer's decode call
+        self.kernel = (kernel, columns, threads)
         self.calls = [(self.x[l].data_ptr(), xd, self.conv_w[l].data_ptr(),
                        self.cache[l].data_ptr(), xd, self.alpha[l].data_ptr(),
                        self.beta[l].data_ptr(), self.state[l].data_ptr(), sd, 1.0,
-                       self.o[l].data_ptr(), M, H, DH, DH, sp) for l in range(L)]
+                       self.o[l].data_ptr(), M, H, DH, DH) for l in range(L)]
+        if kernel == 0:
+            self.fn = self.lib.kda_decode_step
+            self.calls = [c + (sp,) for c in self.calls]
+        else:
+            self.fn = self.lib.kda_decode_step_config
+            self.calls = [c + (kernel, columns, threads, sp) for c in self.calls]
 
     def launch(self, l: int):
-        st = self.lib.kda_decode_step(*self.calls[l])
+        st = self.fn(*self.calls[l])
         if st != 0:
             raise self.kda.KdaError("kda_decode_step", st)
 
@@ -226,29 +240,80 @@ class DecodeStack:
 
 
 def time_device(stack: DecodeStack, K: int, W: int, barrier):
-    """K steps with inputs resident; an event pair around every launch."""
+    """K steps with inputs resident. One step (L launches of the decode
+    kernel through the C ABI) is captured once as a CUDA graph and replayed;
+    an event pair brackets every replay. Returns (total ms, per-step ms)."""
     torch = stack.torch
     with torch.cuda.stream(stack.stream):
-        for _ in range(W):
+        stack.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stack.stream):
             stack.step()
+        for _ in range(W):
+            g.replay()
         torch.cuda.synchronize()
-        n = K * stack.L
-        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
         barrier()
         torch.cuda.synchronize()
-        i = 0
+        ev[0].record(stack.stream)
+        for k in range(K):
+            g.replay()
+            ev[k + 1].record(stack.stream)
+        torch.cuda.synchronize()
+        barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev[:-1], ev[1:])]
+    return ev[0].elapsed_time(ev[-1]), step_ms
+
+
+def time_graph(stack: DecodeStack, K: int, W: int):
+    """K replays of one captured CUDA graph holding a whole step (L launches)."""
+    torch = stack.torch
+    with torch.cuda.stream(stack.stream):
+        stack.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stack.stream):
+            stack.step()
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stack.stream)
         for _ in range(K):
-            for l in range(stack.L):
-                ev0[i].record(stack.stream)
-                stack.launch(l)
-                ev1[i].record(stack.stream)
-                i += 1
+            g.replay()
+        e1.record(stack.stream)
         torch.cuda.synchronize()
-        barrier()
-    total_ms = ev0[0].elapsed_time(ev1[-1])
-    launch_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    return total_ms, launch_ms
+    return e0.elapsed_time(e1)
+
+
+def sweep(args):
+    """34-layer decode stack under a CUDA graph for M in {1,8,16,32,64} and
+    FP32 / BF16 state: one JSON line per point (not the bench's main line)."""
+    import torch
+
+    from linear_attention_decode_step_gb300 import build, inputs, kda
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, kind = measured_peak()
+    Ms = [int(v) for v in args.sweep_m.split(",")]
+    for sd in args.sweep_dtypes.split(","):
+        for M in Ms:
+            stack = DecodeStack(torch, kda, inputs, M, args.layers, sd, args.x_dtype, dev,
+                                kernel=args.kernel, columns=args.columns, threads=args.threads,
+                                replicate=True)
+            K = max(20, min(2000, int(2e5 / M)))
+            ms = time_graph(stack, K, args.warmup)
+            per_layer_us = ms / K / args.layers * 1e3
+            gbs = state_bytes_per_launch(M, sd) / (per_layer_us * 1e-6) / 1e9
+            print(json.dumps({"sweep": True, "M": M, "state_dtype": sd, "layers": args.layers,
+                              "kernel": args.kernel, "columns": args.columns,
+                              "threads": args.threads, "ms_per_stack": ms / K,
+                              "us_per_layer": per_layer_us, "state_gbs": gbs,
+                              "frac_of_%s_hbm" % kind: gbs / peak}), flush=True)
+            del stack
+            torch.cuda.empty_cache()
 
 
 def time_e2e(stack: DecodeStack, K: int, W: int, barrier):
@@ -301,6 +366,7 @@ def config_dict(M, state_dtype, x_dtype, layers=LAYERS):
         "state_dtype": state_dtype, "x_dtype": x_dtype,
         "l2": "inputs larger than L2: each step touches %d layers x %.0f MB of state, "
               "visited in turn" % (layers, state_bytes_per_launch(M, state_dtype) / 2e6),
+        "launch": "one CUDA graph per step holding the %d kda_decode_step launches" % layers,
     }
 
 
@@ -351,10 +417,10 @@ def own_arm(args, rank: int, world: int, local_rank: int):
             dist.barrier()
 
     stack = DecodeStack(torch, kda, inputs, args.M, args.layers, args.state_dtype, args.x_dtype,
-                        dev)
+                        dev, kernel=args.kernel, columns=args.columns, threads=args.threads)
     clocks = ClockSampler(gpu_uuid(torch, dev))
     clocks.start()
-    total_ms, launch_ms = time_device(stack, args.steps, args.warmup, barrier)
+    total_ms, step_ms = time_device(stack, args.steps, args.warmup, barrier)
     clk = clocks.stop()
     e2e_ms = time_e2e(stack, args.steps, max(3, args.warmup // 4), barrier)
 
@@ -369,7 +435,7 @@ def own_arm(args, rank: int, world: int, local_rank: int):
     L = args.layers
     value = world * L * K * sb / (total_ms * 1e-3) / 1e9
     e2e_value = world * L * K * sb / (e2e_ms * 1e-3) / 1e9
-    mean_launch_ms = float(np.mean(launch_ms))
+    mean_launch_ms = total_ms / (K * args.layers)   # launch-to-launch, gaps included
     peak, peak_kind = measured_peak()
     achieved = ab / (mean_launch_ms * 1e-3) / 1e9
     traffic = ncu_traffic_per_launch() if (args.M == 32 and args.state_dtype == "f32") else None
@@ -383,12 +449,17 @@ def own_arm(args, rank: int, world: int, local_rank: int):
         "dtype": "f32" if args.state_dtype == "f32" else "f32 (bf16 state storage)",
         "data": "synthetic", "config": config_dict(args.M, args.state_dtype, args.x_dtype),
         "ms_per_layer": total_ms / K / L,
+        "ms_per_step_spread": [float(np.min(step_ms)), float(np.median(step_ms)),
+                               float(np.max(step_ms))],
         "state_gbs_frac_of_%s_hbm" % peak_kind: value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "kda_decode_kernel", "peak_kind": peak_kind,
+                     "kernel": DECODE_KERNEL if args.kernel in (0, 2) else "kda_decode_kernel",
+                     "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": ab,
-                     "mean_launch_us": mean_launch_ms * 1e3},
+                     "mean_launch_us": mean_launch_ms * 1e3,
+                     "launch_timing": "CUDA events around each replay of a graph of %d launches; "
+                                      "per launch = step time / %d" % (L, L)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": stack.h2d_bytes(),
                 "d2h_bytes_per_step": stack.d2h_bytes()},
         "gpu_launches": K * L,
@@ -415,6 +486,14 @@ def main():
     ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--x-dtype", choices=["f32", "bf16"], default="bf16")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="0 auto, 1 cluster (with --columns/--threads), 2 persistent stream")
+    ap.add_argument("--columns", type=int, default=0)
+    ap.add_argument("--threads", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the 34-layer stack for several M and state dtypes instead")
+    ap.add_argument("--sweep-m", default="1,8,16,32,64")
+    ap.add_argument("--sweep-dtypes", default="f32,bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -425,6 +504,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         reference_arm(args, rank)
+        return
+    if args.sweep:
+        sweep(args)
         return
     if world > 1:
         import torch

@@ -111,20 +111,42 @@ kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w,
                            void *state, int state_dtype, float scale,
                            float *o, int M, int H, int dk, int dv, void *stream);
 
+/* Decode kernels selectable through kda_decode_step_config. */
+typedef enum {
+    KDA_DECODE_AUTO = 0,    /* the library picks (what kda_decode_step does) */
+    KDA_DECODE_CLUSTER = 1, /* one CTA per (stream, head, column slice); the slices of a
+                               head form a thread-block cluster sharing q and k */
+    KDA_DECODE_STREAM = 2   /* persistent: one CTA per SM streams whole heads through a
+                               ring of shared-memory stages filled by bulk copies */
+} kda_decode_kernel;
+
 /*
- * kda_decode_step_tile — kda_decode_step with an explicit work split, for
- * tuning and tests. Each head's dv value columns are split into slices of
- * `columns` (16, 32, 64 or 128), one CTA of `threads` threads each; the
- * slices of one head form a thread-block cluster. kda_decode_step picks the
- * split itself. Unsupported (columns, threads) pairs return
- * KDA_ERR_UNSUPPORTED.
+ * kda_decode_step_config — kda_decode_step with an explicit kernel and work
+ * split, for tuning and tests. With KDA_DECODE_CLUSTER each head's dv value
+ * columns are split into slices of `columns` (16, 32, 64 or 128), one CTA of
+ * `threads` threads each. With KDA_DECODE_STREAM, `columns` is the number of
+ * heads (0-16) whose state is prefetched into L2 ahead of the shared-memory
+ * ring and `threads` the number of consumer groups per CTA (1 or 2; 0 picks
+ * the default).
+ * Unsupported combinations return KDA_ERR_UNSUPPORTED. Same arguments,
+ * layouts and results as kda_decode_step.
  */
-kda_status kda_decode_step_tile(const void *x, int x_dtype, const float *conv_w,
-                                void *conv_cache, int cache_dtype,
-                                const float *alpha, const float *beta,
-                                void *state, int state_dtype, float scale,
-                                float *o, int M, int H, int dk, int dv,
-                                int columns, int threads, void *stream);
+kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_w,
+                                  void *conv_cache, int cache_dtype,
+                                  const float *alpha, const float *beta,
+                                  void *state, int state_dtype, float scale,
+                                  float *o, int M, int H, int dk, int dv,
+                                  int kernel, int columns, int threads, void *stream);
+
+/*
+ * kda_device_error — waits for `stream` (cudaStream_t as void*, NULL = legacy
+ * default stream), then reads and clears the library's device error word.
+ * Returns KDA_ERR_TIMEOUT if a kernel gave up a bounded device-side wait since
+ * the last call (its outputs are then incomplete), KDA_ERR_CUDA if the wait or
+ * the read failed, KDA_OK otherwise. The error word is shared by all streams
+ * of the device.
+ */
+kda_status kda_device_error(void *stream);
 
 #ifdef __cplusplus
 }

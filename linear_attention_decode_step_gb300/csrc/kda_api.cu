@@ -96,14 +96,16 @@ kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w, void *
                                         static_cast<cudaStream_t>(stream)));
 }
 
-kda_status kda_decode_step_tile(const void *x, int x_dtype, const float *conv_w,
-                                void *conv_cache, int cache_dtype, const float *alpha,
-                                const float *beta, void *state, int state_dtype, float scale,
-                                float *o, int M, int H, int dk, int dv, int columns, int threads,
-                                void *stream) {
+kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_w,
+                                  void *conv_cache, int cache_dtype, const float *alpha,
+                                  const float *beta, void *state, int state_dtype, float scale,
+                                  float *o, int M, int H, int dk, int dv, int kernel,
+                                  int columns, int threads, void *stream) {
     const kda_status st = check_decode(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta,
                                        state, state_dtype, o, M, H, dk, dv);
     if (st != KDA_OK) return st;
+    const bool explicit_kernel = kernel != KDA_DECODE_AUTO;
+    if (!explicit_kernel) kda::default_decode_config(M, H, state_dtype, &kernel, &columns, &threads);
     kda::DecodeArgs a;
     a.x = x;
     a.conv_w = conv_w;
@@ -115,8 +117,22 @@ kda_status kda_decode_step_tile(const void *x, int x_dtype, const float *conv_w,
     a.M = M;
     a.H = H;
     a.scale = scale;
-    const cudaError_t e = kda::launch_decode(a, x_dtype, state_dtype, columns, threads,
-                                             static_cast<cudaStream_t>(stream));
+    a.l2_prefetch = kda::kDefaultL2Prefetch;
+    int groups = kda::kDefaultGroups;
+    if (explicit_kernel && kernel == KDA_DECODE_STREAM) {
+        if (columns < 0 || columns > 16) return KDA_ERR_UNSUPPORTED;
+        a.l2_prefetch = columns;
+        if (threads != 0) groups = threads;
+    }
+    cudaError_t e;
+    if (kernel == KDA_DECODE_CLUSTER)
+        e = kda::launch_decode(a, x_dtype, state_dtype, columns, threads,
+                               static_cast<cudaStream_t>(stream));
+    else if (kernel == KDA_DECODE_STREAM)
+        e = kda::launch_decode_stream(a, x_dtype, state_dtype, groups,
+                                      static_cast<cudaStream_t>(stream));
+    else
+        return KDA_ERR_INVALID_ARG;
     if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
     return cuda_status(e);
 }
@@ -125,10 +141,18 @@ kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w, void
                            int cache_dtype, const float *alpha, const float *beta, void *state,
                            int state_dtype, float scale, float *o, int M, int H, int dk, int dv,
                            void *stream) {
-    int columns = 0, threads = 0;
-    kda::default_decode_tile(M, H, state_dtype, &columns, &threads);
-    return kda_decode_step_tile(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta, state,
-                                state_dtype, scale, o, M, H, dk, dv, columns, threads, stream);
+    return kda_decode_step_config(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta, state,
+                                  state_dtype, scale, o, M, H, dk, dv, KDA_DECODE_AUTO, 0, 0,
+                                  stream);
+}
+
+kda_status kda_device_error(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e);
+    unsigned int code = 0;
+    e = kda::take_stream_error(&code);
+    if (e != cudaSuccess) return cuda_status(e);
+    return code ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
 }  // extern "C"

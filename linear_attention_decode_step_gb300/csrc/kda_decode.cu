@@ -21,8 +21,9 @@
 // columns in RPT rows: state loads and stores are 128-bit, a warp touches
 // whole 32-byte sectors, and every state element is read once and written
 // once. The column sums u and w are reduced in registers, then with warp
-// shuffles over the lanes that share a strip, then across warps through
-// shared memory.
+// shuffles over the lanes that share a strip, then across warps: each warp
+// stores its partial sums as contiguous [warp][column] rows, CB column
+// threads add them, form d and o, and publish d for the state update.
 //
 // Conv and normalisation. q and k are needed in full by every slice, but
 // each CTA convolves only its own CB channels of q, k and v, so exactly one
@@ -150,7 +151,9 @@ __global__ void __launch_bounds__(NT) kda_decode_kernel(const DecodeArgs a) {
     __shared__ float s_k[DK];
     __shared__ float s_part[NS * WPC][4];
     __shared__ float s_v[CB];
-    __shared__ float s_red[NW][CB][2];
+    __shared__ __align__(16) float s_ru[NW][CB];
+    __shared__ __align__(16) float s_rw[NW][CB];
+    __shared__ __align__(16) float s_d[CB];
 
     const int slice = static_cast<int>(cluster_rank());
     const int h = blockIdx.y, m = blockIdx.z;
@@ -256,21 +259,38 @@ __global__ void __launch_bounds__(NT) kda_decode_kernel(const DecodeArgs a) {
     }
     if (rw == 0) {
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-            s_red[warp][cg * VEC + c][0] = u[c];
-            s_red[warp][cg * VEC + c][1] = w[c];
+        for (int e = 0; e < VEC / 4; ++e) {
+            reinterpret_cast<float4 *>(&s_ru[warp][cg * VEC])[e] =
+                make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+            reinterpret_cast<float4 *>(&s_rw[warp][cg * VEC])[e] =
+                make_float4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
         }
     }
     __syncthreads();
 
-    // 5. correct: d = beta (v - u); S' = s + k d; 128-bit streaming stores
+    // 5. column threads: d = beta (v - u) and the readout o = scale (w + d (k.q))
+    if (tid < CB) {
+        float ut = 0.f, wt = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) {
+            ut += s_ru[ww][tid];
+            wt += s_rw[ww][tid];
+        }
+        const float d = beta * (s_v[tid] - ut);
+        s_d[tid] = d;
+        a.o[head * DK + slice * CB + tid] = a.scale * fmaf(d, kq, wt);
+    }
+    __syncthreads();
+
+    // 6. correct: S' = s + k d; 128-bit streaming stores
     float dcol[VEC];
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-        float ut = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < NW; ++ww) ut += s_red[ww][cg * VEC + c][0];
-        dcol[c] = beta * (s_v[cg * VEC + c] - ut);
+    for (int e = 0; e < VEC / 4; ++e) {
+        const float4 d4 = reinterpret_cast<const float4 *>(&s_d[cg * VEC])[e];
+        dcol[4 * e] = d4.x;
+        dcol[4 * e + 1] = d4.y;
+        dcol[4 * e + 2] = d4.z;
+        dcol[4 * e + 3] = d4.w;
     }
 #pragma unroll
     for (int p = 0; p < RPT; ++p) {
@@ -279,22 +299,6 @@ __global__ void __launch_bounds__(NT) kda_decode_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int c = 0; c < VEC; ++c) nv[c] = fmaf(kr[p], dcol[c], st[p][c]);
         __stcs(reinterpret_cast<uint4 *>(Sg + (size_t)row * DK), Strip<TS>::pack(nv));
-    }
-
-    // 6. read: o = scale (w + d (k.q)), one writer per strip
-    if (warp == 0 && rw == 0) {
-        float ov[VEC];
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-            float wt = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < NW; ++ww) wt += s_red[ww][cg * VEC + c][1];
-            ov[c] = a.scale * fmaf(dcol[c], kq, wt);
-        }
-        float4 *og = reinterpret_cast<float4 *>(a.o + head * DK + slice * CB + cg * VEC);
-#pragma unroll
-        for (int e = 0; e < VEC / 4; ++e)
-            og[e] = make_float4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
     }
 }
 
@@ -340,15 +344,19 @@ cudaError_t launch_decode(const DecodeArgs &a, int x_dtype, int state_dtype, int
     return launch_typed<float, float>(a, columns, threads, stream);
 }
 
-void default_decode_tile(int M, int H, int state_dtype, int *columns, int *threads) {
-    (void)H;
+void default_decode_config(int M, int H, int state_dtype, int *kernel, int *columns,
+                           int *threads) {
     (void)state_dtype;
-    if (M <= 2) {
-        *columns = 16;
-        *threads = 64;
+    *columns = 32;
+    *threads = 128;
+    if ((long)M * H >= 512) {
+        *kernel = KDA_DECODE_STREAM;
     } else {
-        *columns = 32;
-        *threads = 128;
+        *kernel = KDA_DECODE_CLUSTER;
+        if (M <= 2) {
+            *columns = 16;
+            *threads = 64;
+        }
     }
 }
 

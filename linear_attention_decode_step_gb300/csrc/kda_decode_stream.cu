@@ -1,0 +1,447 @@
+// Persistent, bulk-copy-fed KDA decode step for sm_103a.
+//
+// Same arithmetic as kda_decode.cu (conv + SiLU, L2 norm of q and k, the
+// gated delta rule of "GLM-5.3 deep dive" section 8.2.3 Eq. 1 in the fade /
+// predict / correct / read order of section 8.2.6, readout via
+// o = w + d (k.q)), organised for HBM streaming at large M:
+//
+//  * One CTA per SM loops over whole heads (stream m, head h); a head's state
+//    is one contiguous block (64 KiB FP32, 32 KiB BF16).
+//  * Each head's state, alpha, pre-conv x and conv-cache taps are copied into
+//    a ring of NST shared-memory stages with cp.async.bulk; the copies
+//    complete on the stage's "full" mbarrier (transaction bytes).
+//  * The CTA's 16 warps form G consumer groups (G = 1 or 2) that take heads
+//    in turn (group g: heads g, g + G, ...). A group pulls its stage into
+//    registers and convolves the head's 3 x 128 channels from the same stage;
+//    after one group barrier the stage has been read, and the group's first
+//    thread refills it with the head NST places further on and arrives on the
+//    stage's "issued" mbarrier. With two groups, one group's barriers and
+//    reductions overlap the other's loads and arithmetic.
+//  * Ring protocol. The consumer of head j (stage s = j % NST, use n = j / NST)
+//    waits for the n-th refill of s to have been issued, then for its bytes.
+//    That refill was issued by the consumer of head j - NST, after reading
+//    it; the refill before it was issued by this very group when it consumed
+//    head j - 2 NST. So each wait is for the phase right after one already
+//    observed, and mbarrier phase parities cannot alias.
+//  * There is no separate producer warp (16 warps keep 128 registers per
+//    thread available) and no "stage empty" barrier: the thread that refills
+//    a stage is the one that knows it is free.
+//  * The column sums u = k.s and w = q.s are reduced in registers, across the
+//    lanes sharing a strip (BF16), then across the group's warps: each warp
+//    writes its partial sums as contiguous [warp][column] rows (16-byte
+//    stores, no bank conflicts); 128 threads add the partials of u and
+//    publish d while 128 others add those of w and, after one more barrier,
+//    write o. Every thread reads the d of its strip with one 16-byte load and
+//    writes S' with 128-bit streaming stores straight from registers.
+//  * Optionally the state of the head P places beyond the one being loaded is
+//    prefetched into L2 (cp.async.bulk.prefetch.L2).
+//  * Conv weights and beta of a group's next head are prefetched into
+//    registers one head ahead.
+//  * Launched with programmatic stream serialisation: the kernel waits for
+//    the preceding grid (griddepcontrol.wait) before its first global access,
+//    and lets the next launch in the stream start placing CTAs early, which
+//    hides launch latency between back-to-back layers.
+//
+// Each conv-cache channel belongs to exactly one head, so the cache is read
+// (by the bulk copy) and rewritten (by the consumer) by one CTA only.
+//
+// Every mbarrier wait is bounded (about two seconds of clock cycles); on
+// timeout the thread sets the device error word, waits once more (bounded)
+// for the copy it was waiting on, and returns. kda_device_error() reports it
+// on the host.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+#include "kda_ptx.cuh"
+
+namespace kda {
+
+__device__ unsigned int g_stream_error;
+
+namespace {
+
+constexpr int DK = kHeadDim;
+constexpr float kL2Eps = 1e-6f;
+constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s at 2 GHz)
+constexpr int kSmemLimit = 232448;               // 227 KiB opt-in per CTA
+constexpr int kWarps = 16;
+
+template <typename TS, typename TX, int G>
+struct Cfg {
+    static constexpr int VEC = 16 / (int)sizeof(TS);   // columns per 16-byte strip
+    static constexpr int STRIPS = DK / VEC;            // strips per row (32 or 16)
+    static constexpr int SUBS = 32 / STRIPS;           // rows per warp instruction
+    static constexpr int GROUPS = G;
+    static constexpr int CWARPS = kWarps / G;          // warps per consumer group
+    static constexpr int GT = CWARPS * 32;             // threads per group
+    static constexpr int THREADS = kWarps * 32;
+    static constexpr int RGROUPS = CWARPS * SUBS;
+    static constexpr int RPT = DK / RGROUPS;           // rows per thread
+    static_assert(GT >= 2 * DK, "a group needs 256 threads for the column sums");
+    // stage: state | alpha | x (q,k,v) | cache (q,k,v) x (3 taps)
+    static constexpr int S_BYTES = DK * DK * (int)sizeof(TS);
+    static constexpr int A_OFF = S_BYTES;
+    static constexpr int X_OFF = A_OFF + DK * 4;
+    static constexpr int C_OFF = X_OFF + 3 * DK * (int)sizeof(TX);
+    static constexpr int STAGE = C_OFF + 9 * DK * (int)sizeof(TX);
+    // per group: red_u, red_w [CWARPS][DK] | d [DK] | qk [2][DK] | v [DK]
+    static constexpr int REDW_F = CWARPS * DK;
+    static constexpr int DB_F = 2 * CWARPS * DK;
+    static constexpr int QK_F = DB_F + DK;
+    static constexpr int V_F = QK_F + 2 * DK;
+    static constexpr int WORK_F = V_F + DK;
+    static constexpr int WORK_BYTES = WORK_F * 4;
+    static constexpr int BAR_BYTES = 2 * 8 * 8;        // full[8], issued[8]
+    static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
+    static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
+    static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
+    static_assert(NST >= 2, "at least two stages must fit");
+    static_assert(STAGE % 16 == 0 && WORK_BYTES % 16 == 0, "16-byte alignment");
+};
+
+template <typename TS> struct Strip;
+template <> struct Strip<float> {
+    __device__ __forceinline__ static void unpack(const uint4 &r, float (&f)[4]) {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[4]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+};
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+template <> struct Strip<__nv_bfloat16> {
+    __device__ __forceinline__ static void unpack(const uint4 &r, float (&f)[8]) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[8]) {
+        return make_uint4(bf16x2_rn(f[0], f[1]), bf16x2_rn(f[2], f[3]),
+                          bf16x2_rn(f[4], f[5]), bf16x2_rn(f[6], f[7]));
+    }
+};
+
+__device__ __forceinline__ float widen(float v) { return v; }
+__device__ __forceinline__ float widen(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ void raise_error(unsigned int code) { atomicOr(&g_stream_error, code); }
+
+// conv (kernel 4) + SiLU of one channel from the staged taps; writes the
+// shifted taps (c1, c2, x) back to the global cache.
+template <typename TX>
+__device__ __forceinline__ float conv_stage(const float4 w, const TX *cs, const TX *xs, int X,
+                                            int ch, TX *cg, size_t D) {
+    const TX c0 = cs[(X * 3 + 0) * DK + ch], c1 = cs[(X * 3 + 1) * DK + ch];
+    const TX c2 = cs[(X * 3 + 2) * DK + ch], xt = xs[X * DK + ch];
+    cg[0] = c1;
+    cg[D] = c2;
+    cg[2 * D] = xt;
+    const float pre = w.x * widen(c0) + w.y * widen(c1) + w.z * widen(c2) + w.w * widen(xt);
+    return pre / (1.0f + expf(-pre));
+}
+
+// Prefetches the state of head u into L2.
+template <typename TS>
+__device__ __forceinline__ void prefetch_head(const DecodeArgs &a, int u) {
+    ptx::bulk_prefetch_l2(static_cast<const TS *>(a.state) + (size_t)u * DK * DK,
+                          DK * DK * sizeof(TS));
+}
+
+// Issues the bulk copies of head u into stage `st`, completing on `bar`.
+template <typename TS, typename TX, int G>
+__device__ __forceinline__ void load_head(unsigned char *st, uint64_t *bar, const DecodeArgs &a,
+                                          int u, uint64_t pol) {
+    using C = Cfg<TS, TX, G>;
+    const int H = a.H;
+    const size_t D = (size_t)H * DK;
+    const int m = u / H, h = u - m * H;
+    const TX *x = static_cast<const TX *>(a.x);
+    const TX *cache = static_cast<const TX *>(a.cache);
+    ptx::mbar_arrive_expect_tx(bar, C::STAGE);
+    ptx::bulk_g2s_hint(st, static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES, bar,
+                       pol);
+    ptx::bulk_g2s(st + C::A_OFF, a.alpha + (size_t)u * DK, DK * 4, bar);
+#pragma unroll
+    for (int X = 0; X < 3; ++X)
+        ptx::bulk_g2s(st + C::X_OFF + X * DK * sizeof(TX), x + ((size_t)m * 3 + X) * D + (size_t)h * DK,
+                      DK * sizeof(TX), bar);
+#pragma unroll
+    for (int j = 0; j < 9; ++j)
+        ptx::bulk_g2s(st + C::C_OFF + j * DK * sizeof(TX), cache + ((size_t)m * 9 + j) * D + (size_t)h * DK,
+                      DK * sizeof(TX), bar);
+}
+
+template <typename TS, typename TX, int G>
+__global__ void __launch_bounds__(Cfg<TS, TX, G>::THREADS, 1)
+kda_decode_stream_kernel(const DecodeArgs a) {
+    using C = Cfg<TS, TX, G>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
+    uint64_t *issued = full + 8;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H;
+    const int n_units = a.M * H;
+    const size_t D = (size_t)H * DK;
+    const uint64_t pol = ptx::policy_evict_first();
+    const int P = a.l2_prefetch;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&issued[s], 1);
+        }
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    ptx::grid_dependency_wait();  // the previous grid's writes are visible from here on
+    ptx::launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units) load_head<TS, TX, G>(smem + s * C::STAGE, &full[s], a, u, pol);
+        }
+        for (int j = 0; j < P; ++j) {
+            const int u = blockIdx.x + (C::NST + j) * gridDim.x;
+            if (u < n_units) prefetch_head<TS>(a, u);
+        }
+    }
+
+    const int g = warp / C::CWARPS;            // consumer group
+    const int ct = tid - g * C::GT;            // thread index within the group
+    const int cwarp = ct >> 5;
+    const int strip = lane % C::STRIPS, sub = lane / C::STRIPS;
+    const int rg = cwarp * C::SUBS + sub;
+    const uint32_t bar_id = 1 + g;
+    float *red = reinterpret_cast<float *>(smem + C::NST * C::STAGE + g * C::WORK_BYTES);
+    float *redw = red + C::REDW_F;
+    float *db = red + C::DB_F;
+    float *qkb = red + C::QK_F;
+    float *vb = red + C::V_F;
+    TX *cache = static_cast<TX *>(a.cache);
+    const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
+
+    // conv channels of this thread: c0 = ct and, with 256-thread groups,
+    // c1 = ct + 256 (c < 384 encodes tensor c / 128, channel c % 128)
+    const int c0 = ct, c1 = ct + C::GT;
+    float4 wA = make_float4(0.f, 0.f, 0.f, 0.f), wB = wA;
+    float beta_n = 0.f;
+    auto prefetch = [&](int un) {
+        const size_t hb = (size_t)(un % H) * DK;
+        if (c0 < 3 * DK) wA = __ldg(w4 + (size_t)(c0 / DK) * D + hb + c0 % DK);
+        if (c1 < 3 * DK) wB = __ldg(w4 + (size_t)(c1 / DK) * D + hb + c1 % DK);
+        beta_n = __ldg(a.beta + un);
+    };
+
+    int i = g;
+    int u = blockIdx.x + i * gridDim.x;
+    if (u < n_units) prefetch(u);
+    for (; u < n_units; i += G, u += G * gridDim.x) {
+        const int s = i % C::NST, n = i / C::NST;
+        const int m = u / H, h = u - m * H;
+        const float4 w0 = wA, w1 = wB;
+        const float beta = beta_n;
+        const int un = u + G * gridDim.x;
+        if (un < n_units) prefetch(un);
+
+        if ((n > 0 && !ptx::mbar_wait(&issued[s], (n - 1) & 1, kWaitBudget)) ||
+            !ptx::mbar_wait(&full[s], n & 1, kWaitBudget)) {
+            raise_error(4u);
+            ptx::mbar_wait(&full[s], n & 1, kWaitBudget);
+            return;
+        }
+        const unsigned char *st = smem + s * C::STAGE;
+        const TS *Ss = reinterpret_cast<const TS *>(st);
+        const float *al = reinterpret_cast<const float *>(st + C::A_OFF);
+        const TX *xs = reinterpret_cast<const TX *>(st + C::X_OFF);
+        const TX *cs = reinterpret_cast<const TX *>(st + C::C_OFF);
+
+        // (a) state strips into registers, faded by alpha of their row
+        float sv[C::RPT][C::VEC];
+#pragma unroll
+        for (int p = 0; p < C::RPT; ++p) {
+            const int row = p * C::RGROUPS + rg;
+            const uint4 r = *reinterpret_cast<const uint4 *>(Ss + row * DK + strip * C::VEC);
+            Strip<TS>::unpack(r, sv[p]);
+            const float ar = al[row];
+#pragma unroll
+            for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
+        }
+
+        // (b) conv + SiLU of the head's 384 channels (q, k, v)
+        const size_t cbase = (size_t)m * 9 * D + (size_t)h * DK;
+        if (c0 < 3 * DK) {
+            const int X = c0 / DK, ch = c0 % DK;
+            const float y = conv_stage(w0, cs, xs, X, ch, cache + cbase + 3 * X * D + ch, D);
+            if (X < 2) qkb[X * DK + ch] = y;
+            else vb[ch] = y;
+        }
+        if (c1 < 3 * DK) {
+            const int X = c1 / DK, ch = c1 % DK;
+            const float y = conv_stage(w1, cs, xs, X, ch, cache + cbase + 3 * X * D + ch, D);
+            if (X < 2) qkb[X * DK + ch] = y;
+            else vb[ch] = y;
+        }
+        ptx::named_bar_sync(bar_id, C::GT);  // barrier 1: stage read; q, k, v visible
+        if (ct == 0) {
+            const int ur = blockIdx.x + (i + C::NST) * gridDim.x;  // refill with head i + NST
+            if (ur < n_units) {
+                load_head<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                ptx::mbar_arrive(&issued[s]);
+                const int up = ur + P * gridDim.x;
+                if (P > 0 && up < n_units) prefetch_head<TS>(a, up);
+            }
+        }
+
+        // (c) norms, formed by every warp from shared memory (lane: 4 channels)
+        const float4 q4 = reinterpret_cast<const float4 *>(qkb)[lane];
+        const float4 k4 = reinterpret_cast<const float4 *>(qkb + DK)[lane];
+        float sq = q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w;
+        float sk = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
+        float sqk = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+        }
+        const float rq = 1.0f / sqrtf(sq + kL2Eps);
+        const float rk = 1.0f / sqrtf(sk + kL2Eps);
+        const float kq = sqk * rq * rk;
+
+        // (d) u = k.s, w = q.s over this thread's rows
+        float uu[C::VEC], ww[C::VEC], kr[C::RPT];
+#pragma unroll
+        for (int c = 0; c < C::VEC; ++c) uu[c] = ww[c] = 0.f;
+#pragma unroll
+        for (int p = 0; p < C::RPT; ++p) {
+            const int row = p * C::RGROUPS + rg;
+            kr[p] = qkb[DK + row] * rk;
+            const float qr = qkb[row] * rq;
+#pragma unroll
+            for (int c = 0; c < C::VEC; ++c) {
+                uu[c] = fmaf(kr[p], sv[p][c], uu[c]);
+                ww[c] = fmaf(qr, sv[p][c], ww[c]);
+            }
+        }
+        if (C::SUBS == 2) {
+#pragma unroll
+            for (int c = 0; c < C::VEC; ++c) {
+                uu[c] += __shfl_xor_sync(0xffffffffu, uu[c], 16);
+                ww[c] += __shfl_xor_sync(0xffffffffu, ww[c], 16);
+            }
+        }
+        if (sub == 0) {
+            float4 *ru = reinterpret_cast<float4 *>(red + cwarp * DK + strip * C::VEC);
+            float4 *rw = reinterpret_cast<float4 *>(redw + cwarp * DK + strip * C::VEC);
+#pragma unroll
+            for (int e = 0; e < C::VEC / 4; ++e) {
+                ru[e] = make_float4(uu[4 * e], uu[4 * e + 1], uu[4 * e + 2], uu[4 * e + 3]);
+                rw[e] = make_float4(ww[4 * e], ww[4 * e + 1], ww[4 * e + 2], ww[4 * e + 3]);
+            }
+        }
+        ptx::named_bar_sync(bar_id, C::GT);  // barrier 2: partial column sums
+
+        // (e) threads 0-127 form d_j = beta (v_j - u_j); 128-255 sum w_j
+        float wt = 0.f;
+        if (ct < DK) {
+            float ut = 0.f;
+#pragma unroll
+            for (int q = 0; q < C::CWARPS; ++q) ut += red[q * DK + ct];
+            db[ct] = beta * (vb[ct] - ut);
+        } else if (ct < 2 * DK) {
+#pragma unroll
+            for (int q = 0; q < C::CWARPS; ++q) wt += redw[q * DK + ct - DK];
+        }
+        ptx::named_bar_sync(bar_id, C::GT);  // barrier 3: d published
+        if (ct >= DK && ct < 2 * DK)  // o_j = scale (w_j + d_j (k.q))
+            a.o[(size_t)u * DK + ct - DK] = a.scale * fmaf(db[ct - DK], kq, wt);
+
+        // (f) S' = s + k d, streamed out with 128-bit stores
+        float dd[C::VEC];
+#pragma unroll
+        for (int e = 0; e < C::VEC / 4; ++e) {
+            const float4 d4 = reinterpret_cast<const float4 *>(db + strip * C::VEC)[e];
+            dd[4 * e] = d4.x;
+            dd[4 * e + 1] = d4.y;
+            dd[4 * e + 2] = d4.z;
+            dd[4 * e + 3] = d4.w;
+        }
+        TS *Sg = static_cast<TS *>(a.state) + (size_t)u * DK * DK + strip * C::VEC;
+#pragma unroll
+        for (int p = 0; p < C::RPT; ++p) {
+            const int row = p * C::RGROUPS + rg;
+            float nv[C::VEC];
+#pragma unroll
+            for (int c = 0; c < C::VEC; ++c) nv[c] = fmaf(kr[p], dd[c], sv[p][c]);
+            __stcs(reinterpret_cast<uint4 *>(Sg + (size_t)row * DK), Strip<TS>::pack(nv));
+        }
+    }
+}
+
+template <typename TS, typename TX, int G>
+cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
+    using C = Cfg<TS, TX, G>;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_decode_stream_kernel<TS, TX, G>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const int units = a.M * a.H;
+    const int grid = units < sms ? units : sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_decode_stream_kernel<TS, TX, G>, a);
+}
+
+template <typename TS, typename TX>
+cudaError_t launch_groups(const DecodeArgs &a, int groups, cudaStream_t stream) {
+    if (groups == 1) return launch_stream_typed<TS, TX, 1>(a, stream);
+    if (groups == 2) return launch_stream_typed<TS, TX, 2>(a, stream);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_stream(const DecodeArgs &a, int x_dtype, int state_dtype, int groups,
+                                 cudaStream_t stream) {
+    const bool xb = x_dtype == KDA_BF16, sb = state_dtype == KDA_BF16;
+    if (sb && xb) return launch_groups<__nv_bfloat16, __nv_bfloat16>(a, groups, stream);
+    if (sb) return launch_groups<__nv_bfloat16, float>(a, groups, stream);
+    if (xb) return launch_groups<float, __nv_bfloat16>(a, groups, stream);
+    return launch_groups<float, float>(a, groups, stream);
+}
+
+cudaError_t take_stream_error(unsigned int *code) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_stream_error, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    if (*code) e = cudaMemcpyToSymbol(g_stream_error, &zero, sizeof(unsigned int));
+    return e;
+}
+
+}  // namespace kda

@@ -9,6 +9,8 @@
 namespace kda {
 
 constexpr int kHeadDim = 128;  // dk = dv handled by the decode and prefill kernels
+constexpr int kDefaultL2Prefetch = 0;  // streaming decode: heads prefetched into L2 ahead
+constexpr int kDefaultGroups = 2;      // streaming decode: consumer groups per CTA
 
 // Arguments of one fused decode step (layouts as documented in kda.h).
 struct DecodeArgs {
@@ -21,6 +23,7 @@ struct DecodeArgs {
     float *o;              // [M, H, 128]
     int M, H;
     float scale;
+    int l2_prefetch;       // streaming kernel: heads prefetched into L2 beyond the ring
 };
 
 // Launches the decode kernel for the given storage types and work split.
@@ -29,8 +32,18 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs &a, int x_dtype, int state_dtype,
                           int columns, int threads, cudaStream_t stream);
 
-// Picks the decode work split (columns per CTA, threads per CTA) for M.
-void default_decode_tile(int M, int H, int state_dtype, int *columns, int *threads);
+// Persistent streaming decode kernel (one CTA per SM, bulk-copy stages,
+// `groups` = 1 or 2 consumer groups). cudaErrorNotSupported for other groups.
+cudaError_t launch_decode_stream(const DecodeArgs &a, int x_dtype, int state_dtype, int groups,
+                                 cudaStream_t stream);
+
+// Picks the decode kernel (KDA_DECODE_CLUSTER or KDA_DECODE_STREAM) and, for
+// the cluster kernel, its work split (columns per CTA, threads per CTA).
+void default_decode_config(int M, int H, int state_dtype, int *kernel, int *columns,
+                           int *threads);
+
+// Reads and clears the streaming kernel's device error word.
+cudaError_t take_stream_error(unsigned int *code);
 
 // Standalone short conv + SiLU for one token.
 cudaError_t launch_conv(const void *x, int x_dtype, const float *conv_w, void *cache,

@@ -22,14 +22,16 @@ import torch
 __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_F32", "KDA_BF16",
+    "KDA_DECODE_AUTO", "KDA_DECODE_CLUSTER", "KDA_DECODE_STREAM",
     "KdaError", "lib", "library_path", "header_functions",
     "kda_status_string", "kda_last_cuda_error", "kda_version",
-    "kda_conv_step", "kda_decode_step", "kda_decode_step_tile",
+    "kda_conv_step", "kda_decode_step", "kda_decode_step_config", "kda_device_error",
 ]
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
 KDA_ERR_ALIGNMENT, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_F32, KDA_BF16 = 0, 1
+KDA_DECODE_AUTO, KDA_DECODE_CLUSTER, KDA_DECODE_STREAM = 0, 1, 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _HEADER = os.path.join(os.path.dirname(_PKG), "include", "kda.h")
@@ -46,8 +48,9 @@ _SIGNATURES = {
     "kda_conv_step": ([_V, _I, _V, _V, _I, _V, _I, _I, _V], _I),
     "kda_decode_step": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
                          _I, _I, _I, _I, _V], _I),
-    "kda_decode_step_tile": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
-                              _I, _I, _I, _I, _I, _I, _V], _I),
+    "kda_decode_step_config": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
+                                _I, _I, _I, _I, _I, _I, _I, _V], _I),
+    "kda_device_error": ([_V], _I),
 }
 
 
@@ -174,11 +177,19 @@ def kda_decode_step(x, conv_w, conv_cache, alpha, beta, state, o=None, scale=1.0
     return o
 
 
-def kda_decode_step_tile(x, conv_w, conv_cache, alpha, beta, state, o=None, scale=1.0,
-                         columns=32, threads=128, stream=None):
-    """kda_decode_step with an explicit (columns per CTA, threads per CTA)."""
+def kda_decode_step_config(x, conv_w, conv_cache, alpha, beta, state, o=None, scale=1.0,
+                           kernel=KDA_DECODE_AUTO, columns=0, threads=0, stream=None):
+    """kda_decode_step with an explicit kernel (KDA_DECODE_*) and, for the
+    cluster kernel, (columns per CTA, threads per CTA)."""
     M, H, dk, dv, o, args = _decode_args(x, conv_w, conv_cache, alpha, beta, state, o)
-    st = lib().kda_decode_step_tile(*args, float(scale), _dev(o, "o", torch.float32),
-                                    M, H, dk, dv, int(columns), int(threads), _stream(stream))
-    _check("kda_decode_step_tile", st)
+    st = lib().kda_decode_step_config(*args, float(scale), _dev(o, "o", torch.float32),
+                                      M, H, dk, dv, int(kernel), int(columns), int(threads),
+                                      _stream(stream))
+    _check("kda_decode_step_config", st)
     return o
+
+
+def kda_device_error(stream=None) -> int:
+    """Waits for the stream and returns (and clears) the device error status:
+    KDA_OK or KDA_ERR_TIMEOUT (a bounded device wait gave up)."""
+    return lib().kda_device_error(_stream(stream))

@@ -80,12 +80,18 @@ def test_decode_rejects(K, over, status):
     assert _decode_call(K, **over) == status
 
 
-def test_decode_unsupported_tile(K):
+def test_decode_unsupported_config(K):
     L = K.lib()
-    st = L.kda_decode_step_tile(BASE, 1, BASE + GAP, BASE + 2 * GAP, 1, BASE + 3 * GAP,
-                                BASE + 4 * GAP, BASE + 5 * GAP, 0, 1.0, BASE + 6 * GAP,
-                                4, 64, 128, 128, 48, 96, None)
-    assert st == K.KDA_ERR_UNSUPPORTED
+    args = (BASE, 1, BASE + GAP, BASE + 2 * GAP, 1, BASE + 3 * GAP, BASE + 4 * GAP,
+            BASE + 5 * GAP, 0, 1.0, BASE + 6 * GAP, 4, 64, 128, 128)
+    assert L.kda_decode_step_config(*args, K.KDA_DECODE_CLUSTER, 48, 96, None) \
+        == K.KDA_ERR_UNSUPPORTED
+    assert L.kda_decode_step_config(*args, 7, 0, 0, None) == K.KDA_ERR_INVALID_ARG
+    # streaming kernel: L2 prefetch distance beyond 16, or 3 consumer groups
+    assert L.kda_decode_step_config(*args, K.KDA_DECODE_STREAM, 17, 0, None) \
+        == K.KDA_ERR_UNSUPPORTED
+    assert L.kda_decode_step_config(*args, K.KDA_DECODE_STREAM, 0, 3, None) \
+        == K.KDA_ERR_UNSUPPORTED
 
 
 def test_conv_rejects(K):

@@ -32,17 +32,24 @@ def _tol(state_dtype):
     return TOL_BF16_STATE if state_dtype == "bf16" else TOL_F32_STATE
 
 
-def _run(K, dl: DeviceLayer, steps, scale=1.0, tile=None, graph=False):
+def _run(K, dl: DeviceLayer, steps, scale=1.0, tile=None, kernel=None, stream_cfg=(0, 0)):
+    """tile=(columns, threads) selects the cluster kernel with that split;
+    kernel selects a kernel explicitly (stream_cfg = (L2 prefetch, groups)
+    for the streaming kernel); neither: the library's choice."""
     outs = []
     for t in range(steps):
-        if tile is None:
+        if tile is None and kernel is None:
             K.kda_decode_step(dl.x[t], dl.conv_w, dl.cache, dl.alpha[t], dl.beta[t], dl.state,
                               dl.o, scale=scale)
         else:
-            K.kda_decode_step_tile(dl.x[t], dl.conv_w, dl.cache, dl.alpha[t], dl.beta[t],
-                                   dl.state, dl.o, scale=scale, columns=tile[0], threads=tile[1])
+            kern = K.KDA_DECODE_CLUSTER if tile is not None else kernel
+            cols, thr = tile if tile is not None else stream_cfg
+            K.kda_decode_step_config(dl.x[t], dl.conv_w, dl.cache, dl.alpha[t], dl.beta[t],
+                                     dl.state, dl.o, scale=scale, kernel=kern, columns=cols,
+                                     threads=thr)
         outs.append(dl.o.double().cpu().numpy())
     torch.cuda.synchronize()
+    assert K.kda_device_error() == K.KDA_OK
     return outs
 
 
@@ -97,6 +104,44 @@ def test_M32_one_step(K, state_dtype):
 
 
 TILES = [(16, 64), (32, 64), (32, 128), (64, 128), (64, 256), (128, 256)]
+
+
+@pytest.mark.parametrize("kernel", ["cluster", "stream"])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+def test_each_kernel_M32(K, kernel, state_dtype, x_dtype):
+    """Both decode kernels at M=32 (2048 heads: many heads per CTA for the
+    streaming kernel, so every ring stage is reused), three steps."""
+    inp = inputs.decode_layer(inputs.layer_seed(3, 100), M=32, T=3)
+    dl = DeviceLayer(inp, state_dtype, x_dtype)
+    kern = K.KDA_DECODE_CLUSTER if kernel == "cluster" else K.KDA_DECODE_STREAM
+    outs = _run(K, dl, 3, kernel=kern) if kernel == "stream" else _run(K, dl, 3, tile=(32, 128))
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, _tol(state_dtype))
+
+
+@pytest.mark.parametrize("groups,prefetch", [(1, 0), (2, 0), (2, 3), (1, 2)])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_stream_kernel_ring_configs(K, groups, prefetch, state_dtype):
+    """One or two consumer groups on a ring of 3 (FP32) or 5 (BF16) stages,
+    with and without L2 prefetch: 2048 heads over the SMs reuse every stage
+    many times, so both mbarrier parities and the refill order are exercised."""
+    inp = inputs.decode_layer(inputs.layer_seed(3, 200 + groups), M=32, T=2)
+    dl = DeviceLayer(inp, state_dtype)
+    outs = _run(K, dl, 2, kernel=K.KDA_DECODE_STREAM, stream_cfg=(prefetch, groups))
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, _tol(state_dtype))
+
+
+@pytest.mark.parametrize("M,H", [(1, 1), (1, 5), (3, 7), (1, 64), (5, 64), (7, 61)])
+def test_stream_kernel_small_and_ragged(K, M, H):
+    """Streaming kernel with fewer heads than SMs, odd head counts and a
+    ragged last round of heads."""
+    inp = inputs.decode_layer(300 + M * 100 + H, M=M, H=H, T=2)
+    dl = DeviceLayer(inp, "f32")
+    outs = _run(K, dl, 2, kernel=K.KDA_DECODE_STREAM)
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
 
 
 @pytest.mark.parametrize("tile", TILES)
