@@ -35,6 +35,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from linear_attention_decode_step_gb300 import replicas  # noqa: E402
+
 METRIC = "KDA decode state GB/s & ms/layer at M=32 FP32 (fraction of GB300 HBM peak)"
 UNIT = "GB/s"
 H, DH = 64, 128
@@ -162,7 +164,7 @@ class DecodeStack:
     mirrors of the per-step inputs and outputs for the end-to-end leg."""
 
     def __init__(self, torch, kda, inputs, M, L, state_dtype, x_dtype, device, seed_cfg=3,
-                 kernel=0, columns=0, threads=0, replicate=False):
+                 kernel=0, columns=0, threads=0, replicate=False, rank=0):
         """replicate=True draws one layer's inputs and copies them into every
         layer's buffers (used by the sweep, where only timing matters)."""
         self.torch, self.kda, self.M, self.L = torch, kda, M, L
@@ -170,16 +172,19 @@ class DecodeStack:
         D = H * DH
         xt = torch.bfloat16 if x_dtype == "bf16" else torch.float32
         st = torch.bfloat16 if state_dtype == "bf16" else torch.float32
-        # per-step inputs of all layers in one buffer each (one copy per step)
-        self.x = torch.empty((L, M, 3, D), dtype=xt, device=device)
-        self.alpha = torch.empty((L, M, H, DH), dtype=torch.float32, device=device)
-        self.beta = torch.empty((L, M, H), dtype=torch.float32, device=device)
-        self.o = torch.empty((L, M, H, DH), dtype=torch.float32, device=device)
+        # per-step inputs of all layers in one buffer each (one copy per step);
+        # two sets, so the end-to-end leg can copy step k+1 in while step k runs
+        self.xs = [torch.empty((L, M, 3, D), dtype=xt, device=device) for _ in range(2)]
+        self.alphas = [torch.empty((L, M, H, DH), dtype=torch.float32, device=device)
+                       for _ in range(2)]
+        self.betas = [torch.empty((L, M, H), dtype=torch.float32, device=device) for _ in range(2)]
+        self.os = [torch.empty((L, M, H, DH), dtype=torch.float32, device=device) for _ in range(2)]
+        self.x, self.alpha, self.beta, self.o = self.xs[0], self.alphas[0], self.betas[0], self.os[0]
         self.conv_w, self.cache, self.state = [], [], []
         self.host0 = None
         for l in range(L):
             if l == 0 or not replicate:
-                inp = inputs.decode_layer(inputs.layer_seed(seed_cfg, l), M=M, T=1)
+                inp = inputs.decode_layer(replicas.rank_layer_seed(seed_cfg, l, rank), M=M, T=1)
             if l == 0:
                 self.host0 = inp
             if x_dtype == "bf16":
@@ -193,50 +198,50 @@ class DecodeStack:
             self.conv_w.append(torch.from_numpy(inp["conv_w"]).to(device))
             self.cache.append(cache)
             self.state.append(torch.from_numpy(inp["S0"]).to(device).to(st))
+        self.xs[1].copy_(self.x)
+        self.alphas[1].copy_(self.alpha)
+        self.betas[1].copy_(self.beta)
         self.x_h = self.x.cpu().pin_memory()
         self.alpha_h = self.alpha.cpu().pin_memory()
         self.beta_h = self.beta.cpu().pin_memory()
-        self.o_h = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
+        self.o_h = [torch.empty(self.o.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
         self.stream = torch.cuda.Stream(device=device)
         self.lib = kda.lib()
         sp = self.stream.cuda_stream
         xd = kda.KDA_BF16 if x_dtype == "bf16" else kda.KDA_F32
         sd = kda.KDA_BF16 if state_dtype == "bf16" else kda.KDA_F32
-        # marshalled C-ABI arguments of each layer's decode call
+        # marshalled C-ABI arguments of each layer's decode call, per buffer set
         self.kernel = (kernel, columns, threads)
-        self.calls = [(self.x[l].data_ptr(), xd, self.conv_w[l].data_ptr(),
-                       self.cache[l].data_ptr(), xd, self.alpha[l].data_ptr(),
-                       self.beta[l].data_ptr(), self.state[l].data_ptr(), sd, 1.0,
-                       self.o[l].data_ptr(), M, H, DH, DH) for l in range(L)]
-        if kernel == 0:
-            self.fn = self.lib.kda_decode_step
-            self.calls = [c + (sp,) for c in self.calls]
-        else:
-            self.fn = self.lib.kda_decode_step_config
-            self.calls = [c + (kernel, columns, threads, sp) for c in self.calls]
+        self.fn = self.lib.kda_decode_step if kernel == 0 else self.lib.kda_decode_step_config
+        tail = (sp,) if kernel == 0 else (kernel, columns, threads, sp)
+        self.calls = [[(self.xs[b][l].data_ptr(), xd, self.conv_w[l].data_ptr(),
+                        self.cache[l].data_ptr(), xd, self.alphas[b][l].data_ptr(),
+                        self.betas[b][l].data_ptr(), self.state[l].data_ptr(), sd, 1.0,
+                        self.os[b][l].data_ptr(), M, H, DH, DH) + tail for l in range(L)]
+                      for b in range(2)]
 
-    def launch(self, l: int):
-        st = self.fn(*self.calls[l])
+    def launch(self, l: int, b: int = 0):
+        st = self.fn(*self.calls[b][l])
         if st != 0:
             raise self.kda.KdaError("kda_decode_step", st)
 
-    def step(self):
+    def step(self, b: int = 0):
         for l in range(self.L):
-            self.launch(l)
+            self.launch(l, b)
 
-    def copy_in(self):
-        self.x.copy_(self.x_h, non_blocking=True)
-        self.alpha.copy_(self.alpha_h, non_blocking=True)
-        self.beta.copy_(self.beta_h, non_blocking=True)
+    def copy_in(self, b: int = 0):
+        self.xs[b].copy_(self.x_h, non_blocking=True)
+        self.alphas[b].copy_(self.alpha_h, non_blocking=True)
+        self.betas[b].copy_(self.beta_h, non_blocking=True)
 
-    def copy_out(self):
-        self.o_h.copy_(self.o, non_blocking=True)
+    def copy_out(self, b: int = 0):
+        self.o_h[b].copy_(self.os[b], non_blocking=True)
 
     def h2d_bytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in (self.x_h, self.alpha_h, self.beta_h))
 
     def d2h_bytes(self) -> int:
-        return self.o_h.numel() * self.o_h.element_size()
+        return self.o_h[0].numel() * self.o_h[0].element_size()
 
 
 def time_device(stack: DecodeStack, K: int, W: int, barrier):
@@ -317,26 +322,58 @@ def sweep(args):
 
 
 def time_e2e(stack: DecodeStack, K: int, W: int, barrier):
-    """K steps through the public API: pinned host inputs copied in, 34
-    launches, outputs copied back, every step."""
+    """K steps through the public API with host buffers: every step copies its
+    inputs (x, alpha, beta of all layers) in from pinned host memory, runs the
+    34 kda_decode_step launches (captured once per buffer set as a CUDA graph)
+    and copies o back to pinned host memory. Two buffer sets let the copies of
+    neighbouring steps overlap a step's compute (in on one stream, out on
+    another); the timed region runs from the first copy in to the last copy
+    out."""
     torch = stack.torch
-    with torch.cuda.stream(stack.stream):
-        for _ in range(W):
-            stack.copy_in()
-            stack.step()
-            stack.copy_out()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        e0.record(stack.stream)
-        for _ in range(K):
-            stack.copy_in()
-            stack.step()
-            stack.copy_out()
-        e1.record(stack.stream)
-        torch.cuda.synchronize()
-        barrier()
+    cs, ds, s = torch.cuda.Stream(), torch.cuda.Stream(), stack.stream
+    graphs = []
+    with torch.cuda.stream(s):
+        for b in range(2):
+            stack.step(b)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                stack.step(b)
+            graphs.append(g)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]
+    done = [ev(), ev()]
+    freed = [ev(), ev()]
+
+    def run(n):
+        for k in range(n):
+            b = k & 1
+            if k >= 2:
+                cs.wait_event(freed[b])        # step k-2 is done with buffer set b
+            with torch.cuda.stream(cs):
+                stack.copy_in(b)
+            in_ready[b].record(cs)
+            s.wait_event(in_ready[b])
+            graphs[b].replay()
+            done[b].record(s)
+            ds.wait_event(done[b])
+            with torch.cuda.stream(ds):
+                stack.copy_out(b)
+            freed[b].record(ds)
+
+    run(max(3, W))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(cs)
+    s.wait_event(e0)
+    ds.wait_event(e0)
+    run(K)
+    ds.wait_event(done[(K - 1) & 1])
+    e1.record(ds)
+    torch.cuda.synchronize()
+    barrier()
     return e0.elapsed_time(e1)
 
 
@@ -417,24 +454,24 @@ def own_arm(args, rank: int, world: int, local_rank: int):
             dist.barrier()
 
     stack = DecodeStack(torch, kda, inputs, args.M, args.layers, args.state_dtype, args.x_dtype,
-                        dev, kernel=args.kernel, columns=args.columns, threads=args.threads)
+                        dev, kernel=args.kernel, columns=args.columns, threads=args.threads,
+                        rank=rank)
     clocks = ClockSampler(gpu_uuid(torch, dev))
     clocks.start()
     total_ms, step_ms = time_device(stack, args.steps, args.warmup, barrier)
     clk = clocks.stop()
     e2e_ms = time_e2e(stack, args.steps, max(3, args.warmup // 4), barrier)
 
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    # the job's time is the slowest rank's (the only collective: timing)
+    total_ms, e2e_ms = replicas.max_over_ranks([total_ms, e2e_ms], dist if world > 1 else None,
+                                               device=dev)
 
     K = args.steps
     sb = state_bytes_per_launch(args.M, args.state_dtype)
     ab = algorithmic_bytes_per_launch(args.M, args.state_dtype, args.x_dtype)
     L = args.layers
-    value = world * L * K * sb / (total_ms * 1e-3) / 1e9
-    e2e_value = world * L * K * sb / (e2e_ms * 1e-3) / 1e9
+    value = replicas.job_throughput(L * K * sb, world, total_ms * 1e-3) / 1e9
+    e2e_value = replicas.job_throughput(L * K * sb, world, e2e_ms * 1e-3) / 1e9
     mean_launch_ms = total_ms / (K * args.layers)   # launch-to-launch, gaps included
     peak, peak_kind = measured_peak()
     achieved = ab / (mean_launch_ms * 1e-3) / 1e9
