@@ -354,7 +354,8 @@ def time_e2e(stack: DecodeStack, K: int, W: int, barrier):
                 stack.copy_in(b)
             in_ready[b].record(cs)
             s.wait_event(in_ready[b])
-            graphs[b].replay()
+            with torch.cuda.stream(s):   # replay() launches on the current stream
+                graphs[b].replay()
             done[b].record(s)
             ds.wait_event(done[b])
             with torch.cuda.stream(ds):

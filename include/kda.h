@@ -138,6 +138,46 @@ kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_
                                   float *o, int M, int H, int dk, int dv,
                                   int kernel, int columns, int threads, void *stream);
 
+/* Prefill kernels selectable through kda_chunk_prefill_config. */
+typedef enum {
+    KDA_PREFILL_AUTO = 0,  /* the library picks (what kda_chunk_prefill does) */
+    KDA_PREFILL_SIMT = 1   /* CUDA-core chunk kernel: one CTA per (stream, head, 64 value
+                              columns) walks the sequence chunk by chunk */
+} kda_prefill_kernel;
+
+/*
+ * kda_chunk_prefill — the KDA recurrence over T tokens of post-conv q, k, v,
+ * in the chunkwise WY / UT form ("GLM-5.3 deep dive", section 8.2.5, Eq. 6-9):
+ * per (stream, head) the same result as T consecutive steps of steps 2-4 of
+ * kda_decode_step (L2 norm of q and k, Eq. 1 update, readout), without the
+ * convolution.
+ *
+ *   q, k, v  [M, T, H, dk]  post-conv inputs (qkv_dtype); q and k are
+ *                           L2-normalised inside (eps 1e-6), v is not
+ *   alpha    [M, T, H, dk]  FP32 per-key-channel decay, linear space (0, 1]
+ *   beta     [M, T, H]      FP32 write strength
+ *   state    [M, H, dk, dv] FP32, the state before the first token on entry
+ *                           and after the last token on return (in place)
+ *   o        [M, T, H, dv]  FP32 output, o_t = scale * S_t^T q_t
+ *   chunk    tokens per chunk: 64 (other values return KDA_ERR_UNSUPPORTED)
+ *   dk = dv = 128; 1 <= M, H <= 65535; T >= 1 (a ragged last chunk is fine).
+ * Numerical domain: every per-token log(alpha) above about -5.4 (the model's
+ * gate keeps it above -5), so that decay factors over a 16-token block stay
+ * inside FP32.
+ * o must not overlap any input or the state; the state must not overlap any
+ * input.
+ */
+kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qkv_dtype,
+                             const float *alpha, const float *beta, float *state, float *o,
+                             float scale, int M, int T, int H, int dk, int dv, int chunk,
+                             void *stream);
+
+/* kda_chunk_prefill with an explicit kernel (kda_prefill_kernel). */
+kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v, int qkv_dtype,
+                                    const float *alpha, const float *beta, float *state,
+                                    float *o, float scale, int M, int T, int H, int dk, int dv,
+                                    int chunk, int kernel, void *stream);
+
 /*
  * kda_device_error — waits for `stream` (cudaStream_t as void*, NULL = legacy
  * default stream), then reads and clears the library's device error word.

@@ -58,6 +58,31 @@ kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *c
     return KDA_OK;
 }
 
+kda_status check_prefill(const void *q, const void *k, const void *v, int qkv_dtype,
+                         const float *alpha, const float *beta, const float *state,
+                         const float *o, int M, int T, int H, int dk, int dv, int chunk) {
+    if (!q || !k || !v || !alpha || !beta || !state || !o) return KDA_ERR_INVALID_ARG;
+    if (M <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0 || chunk <= 0)
+        return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(qkv_dtype)) return KDA_ERR_INVALID_ARG;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim || chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (M > 65535 || H > 65535) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
+        !aligned16(beta) || !aligned16(state) || !aligned16(o))
+        return KDA_ERR_ALIGNMENT;
+    const size_t tok = (size_t)M * T * H;
+    const size_t n_qkv = tok * dk * dtype_bytes(qkv_dtype);
+    const size_t n_a = tok * dk * 4, n_b = tok * 4, n_o = tok * dv * 4;
+    const size_t n_s = (size_t)M * H * dk * dv * 4;
+    const void *ins[5] = {q, k, v, alpha, beta};
+    const size_t ns[5] = {n_qkv, n_qkv, n_qkv, n_a, n_b};
+    for (int i = 0; i < 5; ++i)
+        if (overlap(o, n_o, ins[i], ns[i]) || overlap(state, n_s, ins[i], ns[i]))
+            return KDA_ERR_INVALID_ARG;
+    if (overlap(o, n_o, state, n_s)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -144,6 +169,38 @@ kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w, void
     return kda_decode_step_config(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta, state,
                                   state_dtype, scale, o, M, H, dk, dv, KDA_DECODE_AUTO, 0, 0,
                                   stream);
+}
+
+kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v, int qkv_dtype,
+                                    const float *alpha, const float *beta, float *state,
+                                    float *o, float scale, int M, int T, int H, int dk, int dv,
+                                    int chunk, int kernel, void *stream) {
+    const kda_status st =
+        check_prefill(q, k, v, qkv_dtype, alpha, beta, state, o, M, T, H, dk, dv, chunk);
+    if (st != KDA_OK) return st;
+    kda::PrefillArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.state = state;
+    a.o = o;
+    a.M = M;
+    a.T = T;
+    a.H = H;
+    a.scale = scale;
+    if (kernel == KDA_PREFILL_AUTO) kernel = KDA_PREFILL_SIMT;
+    if (kernel != KDA_PREFILL_SIMT) return KDA_ERR_INVALID_ARG;
+    return cuda_status(kda::launch_prefill_simt(a, qkv_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qkv_dtype,
+                             const float *alpha, const float *beta, float *state, float *o,
+                             float scale, int M, int T, int H, int dk, int dv, int chunk,
+                             void *stream) {
+    return kda_chunk_prefill_config(q, k, v, qkv_dtype, alpha, beta, state, o, scale, M, T, H, dk,
+                                    dv, chunk, KDA_PREFILL_AUTO, stream);
 }
 
 kda_status kda_device_error(void *stream) {

@@ -26,6 +26,20 @@ struct DecodeArgs {
     int l2_prefetch;       // streaming kernel: heads prefetched into L2 beyond the ring
 };
 
+// Arguments of one chunked prefill (layouts as documented in kda.h).
+struct PrefillArgs {
+    const void *q, *k, *v;  // [M, T, H, 128] post-conv (qkv dtype)
+    const float *alpha;     // [M, T, H, 128]
+    const float *beta;      // [M, T, H]
+    float *state;           // [M, H, 128, 128] in / out
+    float *o;               // [M, T, H, 128]
+    int M, T, H;
+    float scale;
+};
+
+// Chunked prefill on CUDA cores (64-token chunks, 16-token blocks).
+cudaError_t launch_prefill_simt(const PrefillArgs &a, int qkv_dtype, cudaStream_t stream);
+
 // Launches the decode kernel for the given storage types and work split.
 // Returns cudaErrorNotSupported (without launching) when no kernel is
 // instantiated for (columns, threads).

@@ -23,6 +23,7 @@ __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_F32", "KDA_BF16",
     "KDA_DECODE_AUTO", "KDA_DECODE_CLUSTER", "KDA_DECODE_STREAM",
+    "KDA_PREFILL_AUTO", "KDA_PREFILL_SIMT", "kda_chunk_prefill", "kda_chunk_prefill_config",
     "KdaError", "lib", "library_path", "header_functions",
     "kda_status_string", "kda_last_cuda_error", "kda_version",
     "kda_conv_step", "kda_decode_step", "kda_decode_step_config", "kda_device_error",
@@ -32,6 +33,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
 KDA_ERR_ALIGNMENT, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_F32, KDA_BF16 = 0, 1
 KDA_DECODE_AUTO, KDA_DECODE_CLUSTER, KDA_DECODE_STREAM = 0, 1, 2
+KDA_PREFILL_AUTO, KDA_PREFILL_SIMT = 0, 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _HEADER = os.path.join(os.path.dirname(_PKG), "include", "kda.h")
@@ -51,6 +53,9 @@ _SIGNATURES = {
     "kda_decode_step_config": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
                                 _I, _I, _I, _I, _I, _I, _I, _V], _I),
     "kda_device_error": ([_V], _I),
+    "kda_chunk_prefill": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I, _V], _I),
+    "kda_chunk_prefill_config": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I,
+                                  _I, _V], _I),
 }
 
 
@@ -193,3 +198,36 @@ def kda_device_error(stream=None) -> int:
     """Waits for the stream and returns (and clears) the device error status:
     KDA_OK or KDA_ERR_TIMEOUT (a bounded device wait gave up)."""
     return lib().kda_device_error(_stream(stream))
+
+
+def _prefill_args(q, k, v, alpha, beta, state, o):
+    M, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.dtype != q.dtype or k.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape [M, T, H, 128] and dtype")
+    if o is None:
+        o = torch.empty((M, T, H, dv), dtype=torch.float32, device=q.device)
+    args = [_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dtype_code(q),
+            _dev(alpha, "alpha", torch.float32), _dev(beta, "beta", torch.float32),
+            _dev(state, "state", torch.float32), _dev(o, "o", torch.float32)]
+    return M, T, H, dk, dv, o, args
+
+
+def kda_chunk_prefill(q, k, v, alpha, beta, state, o=None, scale=1.0, chunk=64, stream=None):
+    """Chunked prefill over T tokens (see kda.h). q, k, v [M,T,H,128]
+    (bf16|f32, post-conv), alpha [M,T,H,128] f32, beta [M,T,H] f32, state
+    [M,H,128,128] f32 updated in place; returns o [M,T,H,128] f32."""
+    M, T, H, dk, dv, o, args = _prefill_args(q, k, v, alpha, beta, state, o)
+    st = lib().kda_chunk_prefill(*args, float(scale), M, T, H, dk, dv, int(chunk), _stream(stream))
+    _check("kda_chunk_prefill", st)
+    return o
+
+
+def kda_chunk_prefill_config(q, k, v, alpha, beta, state, o=None, scale=1.0, chunk=64,
+                             kernel=KDA_PREFILL_AUTO, stream=None):
+    """kda_chunk_prefill with an explicit kernel (KDA_PREFILL_*)."""
+    M, T, H, dk, dv, o, args = _prefill_args(q, k, v, alpha, beta, state, o)
+    st = lib().kda_chunk_prefill_config(*args, float(scale), M, T, H, dk, dv, int(chunk),
+                                        int(kernel), _stream(stream))
+    _check("kda_chunk_prefill_config", st)
+    return o

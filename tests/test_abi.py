@@ -116,3 +116,25 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kda, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         kda.lib()
+
+
+def _prefill_call(K, **over):
+    a = dict(q=BASE, k=BASE + GAP, v=BASE + 2 * GAP, qd=K.KDA_BF16, alpha=BASE + 3 * GAP,
+             beta=BASE + 4 * GAP, state=BASE + 5 * GAP, o=BASE + 6 * GAP, scale=1.0,
+             M=4, T=4096, H=64, dk=128, dv=128, chunk=64)
+    a.update(over)
+    return K.lib().kda_chunk_prefill(a["q"], a["k"], a["v"], a["qd"], a["alpha"], a["beta"],
+                                     a["state"], a["o"], a["scale"], a["M"], a["T"], a["H"],
+                                     a["dk"], a["dv"], a["chunk"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(state=None), 1), (dict(T=0), 1),
+    (dict(M=0), 1), (dict(chunk=0), 1), (dict(qd=3), 1),
+    (dict(chunk=32), 2), (dict(dk=64), 2), (dict(dv=256), 2), (dict(H=70000), 2),
+    (dict(alpha=BASE + 3 * GAP + 8), 3), (dict(o=BASE + 6 * GAP + 4), 3),
+    (dict(o=BASE + 16), 1),                 # o overlaps q
+    (dict(state=BASE + 3 * GAP + 64), 1),   # state inside alpha
+])
+def test_prefill_rejects(K, over, status):
+    assert _prefill_call(K, **over) == status

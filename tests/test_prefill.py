@@ -1,0 +1,131 @@
+"""GPU parity of the chunked prefill against the fp64 sequential oracle.
+
+The chunked form must reproduce T sequential steps of the recurrence
+("GLM-5.3 deep dive", section 8.2.5): max |gpu - oracle| / max |oracle|
+<= 5e-3 on every output and on the final state.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from linear_attention_decode_step_gb300 import inputs
+from tests.kda_testlib import bits_to_torch_bf16, rel_err
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from linear_attention_decode_step_gb300 import build
+    build.build()
+    from linear_attention_decode_step_gb300 import kda
+    return kda
+
+
+def _device(p, qkv="bf16"):
+    dev = "cuda"
+    if qkv == "bf16":
+        q, k, v = (bits_to_torch_bf16(p[n + "_bits"], dev) for n in ("q", "k", "v"))
+    else:
+        q, k, v = (torch.from_numpy(p[n]).to(dev) for n in ("q", "k", "v"))
+    alpha = torch.from_numpy(p["alpha"]).to(dev)
+    beta = torch.from_numpy(p["beta"]).to(dev)
+    S = torch.from_numpy(p["S0"]).to(dev).clone()
+    return q, k, v, alpha, beta, S
+
+
+def _run(K, p, qkv="bf16", scale=1.0, kernel=None):
+    q, k, v, alpha, beta, S = _device(p, qkv)
+    if kernel is None:
+        o = K.kda_chunk_prefill(q, k, v, alpha, beta, S, scale=scale)
+    else:
+        o = K.kda_chunk_prefill_config(q, k, v, alpha, beta, S, scale=scale, kernel=kernel)
+    torch.cuda.synchronize()
+    return o.double().cpu().numpy(), S.double().cpu().numpy()
+
+
+def _oracle(p, scale=1.0, heads=None):
+    if heads is None:
+        return oracle.recurrent(p["q"], p["k"], p["v"], p["alpha"], p["beta"], p["S0"],
+                                scale=scale)
+    os_, Ss = [], []
+    for (m, h) in heads:
+        sl = (slice(m, m + 1), slice(None), slice(h, h + 1))
+        o, S = oracle.recurrent(p["q"][sl], p["k"][sl], p["v"][sl], p["alpha"][sl],
+                                p["beta"][sl], p["S0"][m:m + 1, h:h + 1], scale=scale)
+        os_.append(o[0, :, 0])
+        Ss.append(S[0, 0])
+    return os_, Ss
+
+
+@pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 200])
+def test_lengths_and_ragged_chunks(K, T):
+    p = inputs.prefill_problem(4000 + T, M=2, T=T, H=3)
+    o, S = _run(K, p)
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(o, o_ref) <= TOL, rel_err(o, o_ref)
+    assert rel_err(S, S_ref) <= TOL, rel_err(S, S_ref)
+
+
+def test_fp32_inputs_and_scale(K):
+    p = inputs.prefill_problem(4100, M=1, T=130, H=2)
+    scale = 128 ** -0.5
+    o, S = _run(K, p, qkv="f32", scale=scale)
+    o_ref, S_ref = _oracle(p, scale=scale)
+    assert rel_err(o, o_ref) <= TOL
+    assert rel_err(S, S_ref) <= TOL
+
+
+def test_decay_at_gate_floor(K):
+    """alpha just above e^-5, the floor of the model's gate (section 8.2.3):
+    a chunk's summed log-decay reaches about -320, far outside FP32 for a
+    single reference point; the 16-token blocks keep every factor finite."""
+    p = inputs.prefill_problem(4200, M=1, T=150, H=2)
+    rng = np.random.default_rng(4201)
+    p["alpha"] = np.exp(-5.0 + 0.05 * rng.random(p["alpha"].shape)).astype(np.float32)
+    o, S = _run(K, p)
+    o_ref, S_ref = _oracle(p)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    assert rel_err(o, o_ref) <= TOL
+    assert rel_err(S, S_ref) <= TOL
+
+
+def test_slow_decay_long_memory(K):
+    """alpha close to 1 (long memory): the state accumulates over many chunks."""
+    p = inputs.prefill_problem(4300, M=1, T=300, H=2, alpha_mean=7.0)
+    o, S = _run(K, p)
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(o, o_ref) <= TOL
+    assert rel_err(S, S_ref) <= TOL
+
+
+def test_identity_steps_read_state(K):
+    """alpha = 1, beta = 0: the state is unchanged and o_t = S0^T q_t."""
+    p = inputs.prefill_problem(4400, M=1, T=70, H=2)
+    p["alpha"] = np.ones_like(p["alpha"])
+    p["beta"] = np.zeros_like(p["beta"])
+    o, S = _run(K, p)
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(S, p["S0"]) <= 1e-6
+    assert rel_err(o, o_ref) <= TOL
+
+
+def test_config4_full_size_sampled_heads(K):
+    """M=4 streams, T=4096 tokens, 64 heads, chunk 64, BF16 q/k/v, FP32
+    state: the whole problem runs on the GPU; six (stream, head) pairs are
+    checked against 4096 sequential oracle steps each (every output of those
+    heads and their final state)."""
+    p = inputs.prefill_problem(inputs.layer_seed(4, 0), M=4, T=4096, H=64)
+    o, S = _run(K, p)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    heads = [(0, 0), (1, 17), (2, 33), (3, 63), (0, 48), (3, 5)]
+    o_ref, S_ref = _oracle(p, heads=heads)
+    for (m, h), orf, srf in zip(heads, o_ref, S_ref):
+        assert rel_err(o[m, :, h], orf) <= TOL, ((m, h), rel_err(o[m, :, h], orf))
+        assert rel_err(S[m, h], srf) <= TOL, ((m, h), rel_err(S[m, h], srf))
