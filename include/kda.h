@@ -141,8 +141,11 @@ kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_
 /* Prefill kernels selectable through kda_chunk_prefill_config. */
 typedef enum {
     KDA_PREFILL_AUTO = 0,  /* the library picks (what kda_chunk_prefill does) */
-    KDA_PREFILL_SIMT = 1   /* CUDA-core chunk kernel: one CTA per (stream, head, 64 value
+    KDA_PREFILL_SIMT = 1,  /* CUDA-core chunk kernel: one CTA per (stream, head, 64 value
                               columns) walks the sequence chunk by chunk */
+    KDA_PREFILL_TC = 2     /* tensor-core chunk kernel (tcgen05, TF32 operands, FP32
+                              accumulation): one CTA per (stream, head), state kept in
+                              tensor memory for the whole sequence */
 } kda_prefill_kernel;
 
 /*

@@ -190,9 +190,13 @@ kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v,
     a.T = T;
     a.H = H;
     a.scale = scale;
-    if (kernel == KDA_PREFILL_AUTO) kernel = KDA_PREFILL_SIMT;
-    if (kernel != KDA_PREFILL_SIMT) return KDA_ERR_INVALID_ARG;
-    return cuda_status(kda::launch_prefill_simt(a, qkv_dtype, static_cast<cudaStream_t>(stream)));
+    if (kernel == KDA_PREFILL_AUTO) kernel = KDA_PREFILL_TC;
+    if (kernel == KDA_PREFILL_SIMT)
+        return cuda_status(
+            kda::launch_prefill_simt(a, qkv_dtype, static_cast<cudaStream_t>(stream)));
+    if (kernel == KDA_PREFILL_TC)
+        return cuda_status(kda::launch_prefill_tc(a, qkv_dtype, static_cast<cudaStream_t>(stream)));
+    return KDA_ERR_INVALID_ARG;
 }
 
 kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qkv_dtype,
@@ -206,10 +210,12 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qk
 kda_status kda_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);
-    unsigned int code = 0;
+    unsigned int code = 0, code2 = 0;
     e = kda::take_stream_error(&code);
     if (e != cudaSuccess) return cuda_status(e);
-    return code ? KDA_ERR_TIMEOUT : KDA_OK;
+    e = kda::take_prefill_error(&code2);
+    if (e != cudaSuccess) return cuda_status(e);
+    return (code | code2) ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
 }  // extern "C"

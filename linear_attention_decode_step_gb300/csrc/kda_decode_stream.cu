@@ -76,7 +76,6 @@ struct Cfg {
     static constexpr int VEC = 16 / (int)sizeof(TS);   // columns per 16-byte strip
     static constexpr int STRIPS = DK / VEC;            // strips per row (32 or 16)
     static constexpr int SUBS = 32 / STRIPS;           // rows per warp instruction
-    static constexpr int GROUPS = G;
     static constexpr int CWARPS = kWarps / G;          // warps per consumer group
     static constexpr int GT = CWARPS * 32;             // threads per group
     static constexpr int THREADS = kWarps * 32;

@@ -40,6 +40,12 @@ struct PrefillArgs {
 // Chunked prefill on CUDA cores (64-token chunks, 16-token blocks).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, int qkv_dtype, cudaStream_t stream);
 
+// Chunked prefill on the tensor cores (tcgen05, TF32 operands, state in TMEM).
+cudaError_t launch_prefill_tc(const PrefillArgs &a, int qkv_dtype, cudaStream_t stream);
+
+// Reads and clears the tensor-core prefill's device error word.
+cudaError_t take_prefill_error(unsigned int *code);
+
 // Launches the decode kernel for the given storage types and work split.
 // Returns cudaErrorNotSupported (without launching) when no kernel is
 // instantiated for (columns, threads).

@@ -23,7 +23,7 @@ __all__ = [
     "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_F32", "KDA_BF16",
     "KDA_DECODE_AUTO", "KDA_DECODE_CLUSTER", "KDA_DECODE_STREAM",
-    "KDA_PREFILL_AUTO", "KDA_PREFILL_SIMT", "kda_chunk_prefill", "kda_chunk_prefill_config",
+    "KDA_PREFILL_AUTO", "KDA_PREFILL_SIMT", "KDA_PREFILL_TC", "kda_chunk_prefill", "kda_chunk_prefill_config",
     "KdaError", "lib", "library_path", "header_functions",
     "kda_status_string", "kda_last_cuda_error", "kda_version",
     "kda_conv_step", "kda_decode_step", "kda_decode_step_config", "kda_device_error",
@@ -33,7 +33,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
 KDA_ERR_ALIGNMENT, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 3, 4, 5
 KDA_F32, KDA_BF16 = 0, 1
 KDA_DECODE_AUTO, KDA_DECODE_CLUSTER, KDA_DECODE_STREAM = 0, 1, 2
-KDA_PREFILL_AUTO, KDA_PREFILL_SIMT = 0, 1
+KDA_PREFILL_AUTO, KDA_PREFILL_SIMT, KDA_PREFILL_TC = 0, 1, 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _HEADER = os.path.join(os.path.dirname(_PKG), "include", "kda.h")

@@ -40,6 +40,9 @@ def _device(p, qkv="bf16"):
     return q, k, v, alpha, beta, S
 
 
+KERNELS = [1, 2]  # KDA_PREFILL_SIMT, KDA_PREFILL_TC
+
+
 def _run(K, p, qkv="bf16", scale=1.0, kernel=None):
     q, k, v, alpha, beta, S = _device(p, qkv)
     if kernel is None:
@@ -47,6 +50,7 @@ def _run(K, p, qkv="bf16", scale=1.0, kernel=None):
     else:
         o = K.kda_chunk_prefill_config(q, k, v, alpha, beta, S, scale=scale, kernel=kernel)
     torch.cuda.synchronize()
+    assert K.kda_device_error() == K.KDA_OK
     return o.double().cpu().numpy(), S.double().cpu().numpy()
 
 
@@ -64,65 +68,71 @@ def _oracle(p, scale=1.0, heads=None):
     return os_, Ss
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 200])
-def test_lengths_and_ragged_chunks(K, T):
+def test_lengths_and_ragged_chunks(K, T, kernel):
     p = inputs.prefill_problem(4000 + T, M=2, T=T, H=3)
-    o, S = _run(K, p)
+    o, S = _run(K, p, kernel=kernel)
     o_ref, S_ref = _oracle(p)
     assert rel_err(o, o_ref) <= TOL, rel_err(o, o_ref)
     assert rel_err(S, S_ref) <= TOL, rel_err(S, S_ref)
 
 
-def test_fp32_inputs_and_scale(K):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_fp32_inputs_and_scale(K, kernel):
     p = inputs.prefill_problem(4100, M=1, T=130, H=2)
     scale = 128 ** -0.5
-    o, S = _run(K, p, qkv="f32", scale=scale)
+    o, S = _run(K, p, qkv="f32", scale=scale, kernel=kernel)
     o_ref, S_ref = _oracle(p, scale=scale)
     assert rel_err(o, o_ref) <= TOL
     assert rel_err(S, S_ref) <= TOL
 
 
-def test_decay_at_gate_floor(K):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_decay_at_gate_floor(K, kernel):
     """alpha just above e^-5, the floor of the model's gate (section 8.2.3):
     a chunk's summed log-decay reaches about -320, far outside FP32 for a
     single reference point; the 16-token blocks keep every factor finite."""
     p = inputs.prefill_problem(4200, M=1, T=150, H=2)
     rng = np.random.default_rng(4201)
     p["alpha"] = np.exp(-5.0 + 0.05 * rng.random(p["alpha"].shape)).astype(np.float32)
-    o, S = _run(K, p)
+    o, S = _run(K, p, kernel=kernel)
     o_ref, S_ref = _oracle(p)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
     assert rel_err(o, o_ref) <= TOL
     assert rel_err(S, S_ref) <= TOL
 
 
-def test_slow_decay_long_memory(K):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_slow_decay_long_memory(K, kernel):
     """alpha close to 1 (long memory): the state accumulates over many chunks."""
     p = inputs.prefill_problem(4300, M=1, T=300, H=2, alpha_mean=7.0)
-    o, S = _run(K, p)
+    o, S = _run(K, p, kernel=kernel)
     o_ref, S_ref = _oracle(p)
     assert rel_err(o, o_ref) <= TOL
     assert rel_err(S, S_ref) <= TOL
 
 
-def test_identity_steps_read_state(K):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_identity_steps_read_state(K, kernel):
     """alpha = 1, beta = 0: the state is unchanged and o_t = S0^T q_t."""
     p = inputs.prefill_problem(4400, M=1, T=70, H=2)
     p["alpha"] = np.ones_like(p["alpha"])
     p["beta"] = np.zeros_like(p["beta"])
-    o, S = _run(K, p)
+    o, S = _run(K, p, kernel=kernel)
     o_ref, S_ref = _oracle(p)
     assert rel_err(S, p["S0"]) <= 1e-6
     assert rel_err(o, o_ref) <= TOL
 
 
-def test_config4_full_size_sampled_heads(K):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config4_full_size_sampled_heads(K, kernel):
     """M=4 streams, T=4096 tokens, 64 heads, chunk 64, BF16 q/k/v, FP32
     state: the whole problem runs on the GPU; six (stream, head) pairs are
     checked against 4096 sequential oracle steps each (every output of those
     heads and their final state)."""
     p = inputs.prefill_problem(inputs.layer_seed(4, 0), M=4, T=4096, H=64)
-    o, S = _run(K, p)
+    o, S = _run(K, p, kernel=kernel)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
     heads = [(0, 0), (1, 17), (2, 33), (3, 63), (0, 48), (3, 5)]
     o_ref, S_ref = _oracle(p, heads=heads)
