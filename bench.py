@@ -378,6 +378,74 @@ def time_e2e(stack: DecodeStack, K: int, W: int, barrier):
     return e0.elapsed_time(e1)
 
 
+# --------------------------------------------------------------------------- prefill
+def prefill_bytes(M, T, H, qkv_bytes=2):
+    """Algorithmic bytes of one prefill: q, k, v, alpha, beta in, o out,
+    state read and written."""
+    tok = M * T * H
+    return tok * DH * (3 * qkv_bytes + 4 + 4) + tok * 4 + 2 * M * H * DH * DH * 4
+
+
+def prefill_flops(M, T, H, chunk=64):
+    """Dense contraction flops of the chunked form per (stream, head, chunk),
+    counted as the pages count them: two C x C score matrices (2 C^2 d), W and
+    U (2 C^2 d), reading and correcting with the state (2 C d^2), the state
+    update (C d^2): 2 (4 C^2 d + 3 C d^2) = 2 * 5.24 M at C = 64, d = 128."""
+    C = chunk
+    macs = 4 * C * C * DH + 3 * C * DH * DH
+    return 2 * macs * M * H * ((T + C - 1) // C)
+
+
+def time_prefill(torch, kda, inputs, M, T, K, W, kernel=0):
+    """K chunked prefills of one (M, T, 64-head) problem resident on the GPU,
+    timed with CUDA events around the whole run (state updated in place)."""
+    p = inputs.prefill_problem(inputs.layer_seed(4, 0), M=M, T=T, H=H)
+    dev = torch.device("cuda")
+    bf = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    q, k, v = bf(p["q_bits"]), bf(p["k_bits"]), bf(p["v_bits"])
+    alpha = torch.from_numpy(p["alpha"]).to(dev)
+    beta = torch.from_numpy(p["beta"]).to(dev)
+    S = torch.from_numpy(p["S0"]).to(dev)
+    o = torch.empty((M, T, H, DH), dtype=torch.float32, device=dev)
+    del p
+    run = lambda: kda.kda_chunk_prefill_config(q, k, v, alpha, beta, S, o, kernel=kernel)
+    for _ in range(W):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    if kda.kda_device_error() != kda.KDA_OK:
+        raise RuntimeError("prefill kernel reported a device-side timeout")
+    return e0.elapsed_time(e1) / K
+
+
+def prefill_summary(ms, M, T, peak_hbm, peak_bf16, kernel_name):
+    gb = prefill_bytes(M, T, H) / 1e9
+    tflop = prefill_flops(M, T, H) / 1e12
+    tf32_peak = peak_bf16 / 2   # TF32 dense rate is half the BF16 rate (1.1 vs 2.25 PF nominal)
+    return {
+        "workload": "chunked prefill, M=%d streams x T=%d tokens x %d heads, 128x128 FP32 state, "
+                    "BF16 q/k/v, chunk 64" % (M, T, H),
+        "kernel": kernel_name, "ms": ms, "tokens_per_s": M * T / (ms * 1e-3),
+        "gb_s": gb / (ms * 1e-3), "frac_of_measured_hbm": gb / (ms * 1e-3) / peak_hbm,
+        "algorithmic_bytes": gb * 1e9, "tflop_s": tflop / (ms * 1e-3),
+        "frac_of_tf32_peak": tflop / (ms * 1e-3) / tf32_peak,
+        "tf32_peak_tflop_s": tf32_peak, "tf32_peak_kind": "measured bf16 x nominal 1.1/2.25",
+    }
+
+
+def measured_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_decode_sample(inp, budget_s: float):
     """Times the fp64 oracle's decode step on `inp` until budget_s passes
@@ -503,6 +571,12 @@ def own_arm(args, rank: int, world: int, local_rank: int):
         "gpu_launches": K * L,
         "clocks": clk,
     }
+    if not args.no_prefill:
+        pk = {1: "kda_prefill_simt_kernel", 2: "kda_prefill_tc_kernel"}.get(args.prefill_kernel,
+                                                                             "kda_prefill_tc_kernel")
+        pms = time_prefill(torch, kda, inputs, 4, 4096, min(args.steps, 20), 3,
+                           kernel=args.prefill_kernel)
+        line["prefill"] = prefill_summary(pms, 4, 4096, peak, measured_bf16(), pk)
     if world == 1 and not args.no_cpu_baseline:
         gbs, n, el = oracle_decode_sample(stack.host0, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -528,6 +602,13 @@ def main():
                     help="0 auto, 1 cluster (with --columns/--threads), 2 persistent stream")
     ap.add_argument("--columns", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the chunked-prefill measurement")
+    ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor core")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill (with --prefill-M/--prefill-T), one JSON line")
+    ap.add_argument("--prefill-M", type=int, default=4)
+    ap.add_argument("--prefill-T", type=int, default=4096)
     ap.add_argument("--sweep", action="store_true",
                     help="time the 34-layer stack for several M and state dtypes instead")
     ap.add_argument("--sweep-m", default="1,8,16,32,64")
@@ -545,6 +626,17 @@ def main():
         return
     if args.sweep:
         sweep(args)
+        return
+    if args.prefill_only:
+        import torch
+        from linear_attention_decode_step_gb300 import build, inputs, kda
+        build.build()
+        torch.cuda.set_device(0)
+        pms = time_prefill(torch, kda, inputs, args.prefill_M, args.prefill_T, args.steps,
+                           args.warmup, kernel=args.prefill_kernel)
+        peak, _ = measured_peak()
+        print(json.dumps(prefill_summary(pms, args.prefill_M, args.prefill_T, peak,
+                                         measured_bf16(), "kernel %d" % args.prefill_kernel)))
         return
     if world > 1:
         import torch

@@ -125,14 +125,23 @@ __device__ __forceinline__ void load4(const float *p, float (&f)[4]) {
 __device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
 
+// FP32 -> TF32, round to nearest (ties away). The tensor cores read an FP32
+// operand as TF32 by ignoring its low 13 mantissa bits, a biased truncation;
+// operands written here are rounded first so their errors stay unbiased.
+__device__ __forceinline__ float tf32r(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+    return __uint_as_float(y);
+}
+
 __device__ __forceinline__ void st_tile4(unsigned char *tile, uint32_t row, uint32_t c4,
                                          uint32_t kbytes, float a, float b, float c, float d) {
     *reinterpret_cast<float4 *>(tile + (row >> 3) * (8u * kbytes) + c4 * 128u + (row & 7u) * 16u) =
-        make_float4(a, b, c, d);
+        make_float4(tf32r(a), tf32r(b), tf32r(c), tf32r(d));
 }
 __device__ __forceinline__ void st_tile1(unsigned char *tile, uint32_t row, uint32_t k,
                                          uint32_t kbytes, float v) {
-    *reinterpret_cast<float *>(tile + umma::kmajor_offset(row, k, 4, kbytes)) = v;
+    *reinterpret_cast<float *>(tile + umma::kmajor_offset(row, k, 4, kbytes)) = tf32r(v);
 }
 
 // Per-thread inputs of one chunk: rows r = 8 rg + rr, channels 4 c4 + e.
@@ -495,7 +504,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             umma::ld_x8(tq + TM_D3 + 32 * hw + i, y8);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y8[e] = R.v[i + e] - y8[e];
+            for (int e = 0; e < 8; ++e) y8[e] = tf32r(R.v[i + e] - y8[e]);
             umma::st_x8(tq + TM_Z + 32 * hw + i, y8);
         }
         for (int c = 64 * hw; c < 64 * hw + 64; c += 8) {  // S^T[j][c] *= e^{G63_c}
