@@ -80,7 +80,9 @@ constexpr uint32_t T_A = T_P + 64 * KB64;          // A (plain [64][68] FP32)
 constexpr int LDA = 68;
 constexpr uint32_t T_T = T_A + 64 * LDA * 4;       // T = (I + A)^-1 (plain [64][68] FP32)
 constexpr uint32_t T_X = T_T + 64 * LDA * 4;       // scratch: up to 3 blocks of 16 x 16
-constexpr uint32_t PH2_END = T_X + 3 * 256 * 4;
+constexpr int LDK = 144;                           // Kdec staging row: 128 + 16 (bank shift)
+constexpr uint32_t T_KST = T_X + 3 * 256 * 4;      // Kdec, token-major staging [64][LDK]
+constexpr uint32_t PH2_END = T_KST + 64 * LDK * 4;
 constexpr uint32_t TILES = PH2_END > PH1_END ? PH2_END : PH1_END;
 // small buffers (bytes)
 constexpr uint32_t S_NORM = TILES;                 // [2][8][64] partial sums of q^2, k^2
@@ -125,13 +127,13 @@ __device__ __forceinline__ void load4(const float *p, float (&f)[4]) {
 __device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
 
-// FP32 -> TF32, round to nearest (ties away). The tensor cores read an FP32
-// operand as TF32 by ignoring its low 13 mantissa bits, a biased truncation;
-// operands written here are rounded first so their errors stay unbiased.
+// FP32 -> TF32, round to nearest (ties away from zero), by adding half a
+// TF32 ulp to the magnitude bits and clearing the 13 bits TF32 drops. The
+// tensor cores read an FP32 operand as TF32 by ignoring those bits, a biased
+// truncation; operands written here are rounded first so their errors stay
+// unbiased. (Inputs are finite; nothing here rounds into inf or NaN.)
 __device__ __forceinline__ float tf32r(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return __uint_as_float(y);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 __device__ __forceinline__ void st_tile4(unsigned char *tile, uint32_t row, uint32_t c4,
@@ -144,16 +146,57 @@ __device__ __forceinline__ void st_tile1(unsigned char *tile, uint32_t row, uint
     *reinterpret_cast<float *>(tile + umma::kmajor_offset(row, k, 4, kbytes)) = tf32r(v);
 }
 
-// Per-thread inputs of one chunk: rows r = 8 rg + rr, channels 4 c4 + e.
-struct ChunkRegs {
-    float q[8][4], k[8][4], la[8][4];  // la: log2(alpha)
-    float v[32];                        // v[r][j], r = 32 hw + i, j = 32 q4 + lane
-    float beta;                         // beta of token tid (tid < 64)
+// Per-thread inputs of one chunk, kept exactly as loaded (no arithmetic on
+// them until the chunk is processed, so the loads overlap the previous
+// chunk's work): rows r = 8 rg + rr, channels 4 c4 + e.
+template <typename TQ> struct Raw;
+template <> struct Raw<__nv_bfloat16> {
+    typedef uint2 Q4;              // 4 BF16
+    typedef unsigned short V1;     // 1 BF16
+    __device__ __forceinline__ static Q4 load4(const __nv_bfloat16 *p) {
+        return __ldg(reinterpret_cast<const uint2 *>(p));
+    }
+    __device__ __forceinline__ static void widen4(const Q4 &u, float (&f)[4]) {
+        f[0] = __uint_as_float(u.x << 16);
+        f[1] = __uint_as_float(u.x & 0xffff0000u);
+        f[2] = __uint_as_float(u.y << 16);
+        f[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+    __device__ __forceinline__ static V1 load1(const __nv_bfloat16 *p) {
+        return __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+    __device__ __forceinline__ static float widen1(V1 v) { return __uint_as_float((uint32_t)v << 16); }
+    __device__ __forceinline__ static V1 zero1() { return 0; }
+};
+template <> struct Raw<float> {
+    typedef float4 Q4;
+    typedef float V1;
+    __device__ __forceinline__ static Q4 load4(const float *p) {
+        return __ldg(reinterpret_cast<const float4 *>(p));
+    }
+    __device__ __forceinline__ static void widen4(const Q4 &u, float (&f)[4]) {
+        f[0] = u.x;
+        f[1] = u.y;
+        f[2] = u.z;
+        f[3] = u.w;
+    }
+    __device__ __forceinline__ static V1 load1(const float *p) { return __ldg(p); }
+    __device__ __forceinline__ static float widen1(V1 v) { return v; }
+    __device__ __forceinline__ static V1 zero1() { return 0.f; }
 };
 
 template <typename TQ>
-__device__ __forceinline__ void load_chunk(ChunkRegs &R, const PrefillArgs &a, int m, int h, int c0,
-                                           int rr, int c4, int q4, int hw, int lane, int tid) {
+struct ChunkRegs {
+    typename Raw<TQ>::Q4 q[8], k[8];
+    float4 al[8];                      // alpha (linear); 1 on padding rows
+    typename Raw<TQ>::V1 v[32];        // v[r][j], r = 32 hw + i, j = 32 q4 + lane
+    float beta;                        // beta of token tid (tid < 64)
+};
+
+template <typename TQ>
+__device__ __forceinline__ void load_chunk(ChunkRegs<TQ> &R, const PrefillArgs &a, int m, int h,
+                                           int c0, int rr, int c4, int q4, int hw, int lane, int tid) {
+    using RW = Raw<TQ>;
     const TQ *q = static_cast<const TQ *>(a.q);
     const TQ *k = static_cast<const TQ *>(a.k);
     const TQ *v = static_cast<const TQ *>(a.v);
@@ -163,21 +206,19 @@ __device__ __forceinline__ void load_chunk(ChunkRegs &R, const PrefillArgs &a, i
         const int t = c0 + 8 * rg + rr;
         if (t < T) {
             const size_t base = (((size_t)m * T + t) * H + h) * DK + 4 * c4;
-            load4(q + base, R.q[rg]);
-            load4(k + base, R.k[rg]);
-            float al[4];
-            load4(a.alpha + base, al);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) R.la[rg][e] = lg2(al[e]);
+            R.q[rg] = RW::load4(q + base);
+            R.k[rg] = RW::load4(k + base);
+            R.al[rg] = __ldg(reinterpret_cast<const float4 *>(a.alpha + base));
         } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) R.q[rg][e] = R.k[rg][e] = R.la[rg][e] = 0.f;
+            R.q[rg] = R.k[rg] = typename RW::Q4{};
+            R.al[rg] = make_float4(1.f, 1.f, 1.f, 1.f);
         }
     }
-#pragma unroll 8
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int t = c0 + 32 * hw + i;
-        R.v[i] = t < T ? load1(v + (((size_t)m * T + t) * H + h) * DK + 32 * q4 + lane) : 0.f;
+        R.v[i] = t < T ? RW::load1(v + (((size_t)m * T + t) * H + h) * DK + 32 * q4 + lane)
+                       : RW::zero1();
     }
     if (tid < C) {
         const int t = c0 + tid;
@@ -196,6 +237,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     float *sA = reinterpret_cast<float *>(sm + T_A);
     float *sT = reinterpret_cast<float *>(sm + T_T);
     float *sX = reinterpret_cast<float *>(sm + T_X);
+    float *sKst = reinterpret_cast<float *>(sm + T_KST);
 
     const int h = blockIdx.x % a.H, m = blockIdx.x / a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,7 +271,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     }
     umma::wait_st();
 
-    ChunkRegs R;
+    using RW = Raw<TQ>;
+    ChunkRegs<TQ> R;
     load_chunk<TQ>(R, a, m, h, 0, rr, c4, q4, hw, lane, tid);
 
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
@@ -241,13 +284,22 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     for (int c0 = 0; c0 < T && ok; c0 += C, phase ^= 1) {
         // ---------------------------------------------------------- 1. decay, norms
         // cumulative log2-decay over the chunk's rows (rows across lanes rr, then rg)
-        float G[8][4];
+        float G[8][4], qf[8][4], kf[8][4];
+#pragma unroll
+        for (int rg = 0; rg < 8; ++rg) {
+            RW::widen4(R.q[rg], qf[rg]);
+            RW::widen4(R.k[rg], kf[rg]);
+            G[rg][0] = lg2(R.al[rg].x);
+            G[rg][1] = lg2(R.al[rg].y);
+            G[rg][2] = lg2(R.al[rg].z);
+            G[rg][3] = lg2(R.al[rg].w);
+        }
         float carry[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int rg = 0; rg < 8; ++rg) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float x = R.la[rg][e];
+                float x = G[rg][e];
 #pragma unroll
                 for (int d = 4; d < 32; d <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, d);
@@ -272,8 +324,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                sq = fmaf(R.q[rg][e], R.q[rg][e], sq);
-                sk = fmaf(R.k[rg][e], R.k[rg][e], sk);
+                sq = fmaf(qf[rg][e], qf[rg][e], sq);
+                sk = fmaf(kf[rg][e], kf[rg][e], sk);
             }
             sq += __shfl_xor_sync(0xffffffffu, sq, 1);
             sq += __shfl_xor_sync(0xffffffffu, sq, 2);
@@ -317,11 +369,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             float L[4], Lq[4], Rr[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float u = ex2(G[rg][e] - (second ? m1[e] : m0[e]));
-                const float kh = R.k[rg][e] * rk[rg], qh = R.q[rg][e] * rq[rg];
+                const float x = G[rg][e] - (second ? m1[e] : m0[e]);
+                const float u = ex2(x), ui = ex2(-x);
+                const float kh = kf[rg][e] * rk[rg], qh = qf[rg][e] * rq[rg];
                 L[e] = kh * u;
                 Lq[e] = qh * u;
-                Rr[e] = kh / u;
+                Rr[e] = kh * ui;
             }
             const int rowL = second ? r + 32 : r, rowLq = second ? r + 64 : r + 32;
             st_tile4(sm + T_LA, rowL, c4, KB128, L[0], L[1], L[2], L[3]);
@@ -376,24 +429,26 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
             if (active) {
                 const float br = sBeta[r];
+                float d[32];
+                umma::ld_x32(tq + col, d);
+                umma::wait_ld();
 #pragma unroll
-                for (int cb = 0; cb < 32; cb += 8) {
-                    float d8[8];
-                    umma::ld_x8(tq + col + cb, d8);
-                    umma::wait_ld();
+                for (int cb = 0; cb < 32; cb += 4) {
+                    float v4[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < 4; ++e) {
                         const int i = i0 + cb + e;
-                        if (isP) {
-                            st_tile1(sm + T_P, r, i, KB64, i <= r ? d8[e] : 0.f);
-                        } else {
-                            sA[r * LDA + i] = i < r ? br * d8[e] : 0.f;
-                        }
+                        v4[e] = isP ? (i <= r ? d[cb + e] : 0.f) : (i < r ? br * d[cb + e] : 0.f);
                     }
+                    if (isP)
+                        st_tile4(sm + T_P, r, (i0 + cb) >> 2, KB64, v4[0], v4[1], v4[2], v4[3]);
+                    else
+                        *reinterpret_cast<float4 *>(sA + r * LDA + i0 + cb) =
+                            make_float4(v4[0], v4[1], v4[2], v4[3]);
                 }
             } else if (q4 == 3) {  // P rows 0-31, columns 32-63 are zero
-#pragma unroll 4
-                for (int i = 32; i < 64; ++i) st_tile1(sm + T_P, lane, i, KB64, 0.f);
+#pragma unroll
+                for (int cb = 32; cb < 64; cb += 4) st_tile4(sm + T_P, lane, cb >> 2, KB64, 0.f, 0.f, 0.f, 0.f);
             }
         }
         umma::fence_before_sync();
@@ -414,19 +469,33 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             for (int rg = 0; rg < 8; ++rg) {
                 const int r = 8 * rg + rr;
                 const bool second = rg >= 4;
-                float Kd[4], Qd[4];
+                float Kd[4], Qd[4], Kc[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float u = ex2(G[rg][e] - (second ? m1[e] : m0[e]));
-                    const float kh = R.k[rg][e] * rk[rg], qh = R.q[rg][e] * rq[rg];
+                    const float x = G[rg][e] - (second ? m1[e] : m0[e]);
+                    const float u = ex2(x), ui = ex2(-x);
+                    const float kh = kf[rg][e] * rk[rg], qh = qf[rg][e] * rq[rg];
                     const float em = second ? em1[e] : em0[e];
                     Kd[e] = kh * u * em;
                     Qd[e] = qh * u * em;
-                    st_tile1(sm + T_KDEC, 4 * c4 + e, r, KB64, (kh / u) * (second ? ed1[e] : ed0[e]));
+                    Kc[e] = kh * ui * (second ? ed1[e] : ed0[e]);
                 }
                 st_tile4(sm + T_KQ, r, c4, KB128, Kd[0], Kd[1], Kd[2], Kd[3]);
                 st_tile4(sm + T_KQ, 64 + r, c4, KB128, Qd[0], Qd[1], Qd[2], Qd[3]);
+                *reinterpret_cast<float4 *>(sKst + r * LDK + 4 * c4) =
+                    make_float4(Kc[0], Kc[1], Kc[2], Kc[3]);
             }
+        }
+        __syncthreads();
+        // Kdec^T tile (row = key channel c, K = token): 16-byte row segments,
+        // 8 consecutive channels per quarter-warp (one core matrix)
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int u = it * NT + tid;
+            const int c8 = u & 7, kq = (u >> 3) & 15, cg = u >> 7;
+            const int c = 8 * cg + c8;
+            st_tile4(sm + T_KDEC, c, kq, KB64, sKst[(4 * kq + 0) * LDK + c], sKst[(4 * kq + 1) * LDK + c],
+                     sKst[(4 * kq + 2) * LDK + c], sKst[(4 * kq + 3) * LDK + c]);
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
@@ -461,33 +530,51 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         //     T_RI = -T_RR X_RI,  X_RI = sum_{Q=I}^{R-1} A_RQ T_QI
         for (int d = 1; d < 4; ++d) {
             const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += NT) {
-                const int I = e >> 8, Rb = I + d, r16 = (e >> 4) & 15, c16 = e & 15;
-                float acc = 0.f;
+            // unit: block I (R = I + d), row r16, four columns 4 q16 .. + 3
+            const int I = tid >> 6, r16 = (tid >> 2) & 15, q16 = tid & 3, Rb = I + d;
+            if (I < nblk) {
+                float x4[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int Q = I; Q < Rb; ++Q) {
-#pragma unroll 8
-                    for (int t = 0; t < 16; ++t)
-                        acc = fmaf(sA[(16 * Rb + r16) * LDA + 16 * Q + t],
-                                   sT[(16 * Q + t) * LDA + 16 * I + c16], acc);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const float av = sA[(16 * Rb + r16) * LDA + 16 * Q + t];
+                        const float4 tv =
+                            *reinterpret_cast<const float4 *>(sT + (16 * Q + t) * LDA + 16 * I + 4 * q16);
+                        x4[0] = fmaf(av, tv.x, x4[0]);
+                        x4[1] = fmaf(av, tv.y, x4[1]);
+                        x4[2] = fmaf(av, tv.z, x4[2]);
+                        x4[3] = fmaf(av, tv.w, x4[3]);
+                    }
                 }
-                sX[e] = acc;
+                *reinterpret_cast<float4 *>(sX + (I * 16 + r16) * 16 + 4 * q16) =
+                    make_float4(x4[0], x4[1], x4[2], x4[3]);
             }
             __syncthreads();
-            for (int e = tid; e < nblk * 256; e += NT) {
-                const int I = e >> 8, Rb = I + d, r16 = (e >> 4) & 15, c16 = e & 15;
-                float acc = 0.f;
-#pragma unroll 8
-                for (int t = 0; t < 16; ++t)
-                    acc = fmaf(sT[(16 * Rb + r16) * LDA + 16 * Rb + t], sX[(I * 16 + t) * 16 + c16],
-                               acc);
-                sT[(16 * Rb + r16) * LDA + 16 * I + c16] = -acc;
+            if (I < nblk) {
+                float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const float tv = sT[(16 * Rb + r16) * LDA + 16 * Rb + t];
+                    const float4 xv = *reinterpret_cast<const float4 *>(sX + (I * 16 + t) * 16 + 4 * q16);
+                    t4[0] = fmaf(tv, xv.x, t4[0]);
+                    t4[1] = fmaf(tv, xv.y, t4[1]);
+                    t4[2] = fmaf(tv, xv.z, t4[2]);
+                    t4[3] = fmaf(tv, xv.w, t4[3]);
+                }
+                *reinterpret_cast<float4 *>(sT + (16 * Rb + r16) * LDA + 16 * I + 4 * q16) =
+                    make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
             }
             __syncthreads();
         }
         // 5c. M[r][i] = T[r][i] beta_i (lower with diagonal) into the operand tile
-        for (int e = tid; e < C * C; e += NT) {
-            const int r = e >> 6, i = e & 63;
-            st_tile1(sm + T_M, r, i, KB64, i <= r ? sT[r * LDA + i] * sBeta[i] : 0.f);
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int u = it * NT + tid;
+            const int r = 8 * (u >> 7) + (u & 7), iq = (u >> 3) & 15, i = 4 * iq;
+            const float4 tv = *reinterpret_cast<const float4 *>(sT + r * LDA + i);
+            const float4 bv = *reinterpret_cast<const float4 *>(sBeta + i);
+            st_tile4(sm + T_M, r, iq, KB64, i <= r ? tv.x * bv.x : 0.f, i + 1 <= r ? tv.y * bv.y : 0.f,
+                     i + 2 <= r ? tv.z * bv.z : 0.f, i + 3 <= r ? tv.w * bv.w : 0.f);
         }
         umma::fence_smem_to_async();
 
@@ -498,22 +585,22 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             break;
         }
         umma::fence_after_sync();
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) {  // rows r = 32 hw + i .. + 7
-            float y8[8];
-            umma::ld_x8(tq + TM_D3 + 32 * hw + i, y8);
+        {
+            float y[32];  // rows r = 32 hw .. 32 hw + 31
+            umma::ld_x32(tq + TM_D3 + 32 * hw, y);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y8[e] = tf32r(R.v[i + e] - y8[e]);
-            umma::st_x8(tq + TM_Z + 32 * hw + i, y8);
+            for (int e = 0; e < 32; ++e) y[e] = tf32r(RW::widen1(R.v[e]) - y[e]);
+            umma::st_x32(tq + TM_Z + 32 * hw, y);
         }
-        for (int c = 64 * hw; c < 64 * hw + 64; c += 8) {  // S^T[j][c] *= e^{G63_c}
-            float s8[8];
-            umma::ld_x8(tq + TM_S + c, s8);
+#pragma unroll
+        for (int c = 64 * hw; c < 64 * hw + 64; c += 32) {  // S^T[j][c] *= e^{G63_c}
+            float s32[32];
+            umma::ld_x32(tq + TM_S + c, s32);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s8[e] *= sGam[c + e];
-            umma::st_x8(tq + TM_S + c, s8);
+            for (int e = 0; e < 32; ++e) s32[e] *= sGam[c + e];
+            umma::st_x32(tq + TM_S + c, s32);
         }
         umma::wait_st();
 
@@ -551,15 +638,14 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_after_sync();
 
         // ---------------------------------------------------------- 7. O out
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-            float o8[8];
-            umma::ld_x8(tq + TM_D3 + 64 + 32 * hw + i, o8);
+        {
+            float o32[32];
+            umma::ld_x32(tq + TM_D3 + 64 + 32 * hw, o32);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = c0 + 32 * hw + i + e;
-                if (t < T) a.o[(((size_t)m * T + t) * a.H + h) * DK + j] = a.scale * o8[e];
+            for (int e = 0; e < 32; ++e) {
+                const int t = c0 + 32 * hw + e;
+                if (t < T) a.o[(((size_t)m * T + t) * a.H + h) * DK + j] = a.scale * o32[e];
             }
         }
         umma::fence_before_sync();
