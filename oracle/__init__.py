@@ -33,12 +33,21 @@ __all__ = [
     "recurrent",
     "decode_step",
     "chunk_prefill",
+    "forget_gate",
+    "gated_rmsnorm",
+    "decode_step_fused",
     "L2_EPS",
+    "GATE_LOWER_BOUND",
+    "NORM_EPS",
 ]
 
 #: eps inside the root of the L2 normalisation ("GLM-5.3 deep dive", 8.2.6,
 #: implementation notes: epsilon 1e-6)
 L2_EPS = 1e-6
+#: lower bound of the forget gate, log-space ("GLM-5.3 deep dive", 8.2.3)
+GATE_LOWER_BOUND = -5.0
+#: eps of the gated RMSNorm on the output ("GLM-5.3 deep dive", 8.2.4 notes)
+NORM_EPS = 1e-5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
@@ -67,8 +76,11 @@ def bind(path: str):
                                          I, I, I, I, I, Dd, I, Dd]
     lib.kda_oracle_decode_step.argtypes = [P, P, P, P, P, P, P,
                                            I, I, I, Dd, Dd]
+    lib.kda_oracle_forget_gate.argtypes = [P, P, P, Dd, P, I, I, I]
+    lib.kda_oracle_gated_rmsnorm.argtypes = [P, P, P, Dd, P, I, I, I]
     for f in (lib.kda_oracle_conv_step, lib.kda_oracle_recurrent,
-              lib.kda_oracle_decode_step):
+              lib.kda_oracle_decode_step, lib.kda_oracle_forget_gate,
+              lib.kda_oracle_gated_rmsnorm):
         f.restype = None
     return lib
 
@@ -135,6 +147,48 @@ def decode_step(x, w, cache, alpha, beta, S0, scale=1.0, eps=L2_EPS):
     o = np.empty((M, H, d), dtype=np.float64)
     _load().kda_oracle_decode_step(_p(x), _p(w), _p(cache), _p(alpha), _p(beta),
                                    _p(S), _p(o), M, H, d, float(scale), float(eps))
+    return o, S, cache
+
+
+def forget_gate(f, A_log, dt_bias, lb=GATE_LOWER_BOUND):
+    """alpha = exp(lb * sigmoid(exp(A_h) (f + b_{h,c}))).
+
+    f [M,H,dk] (or [M,T,H,dk] flattened the same way), A_log [H],
+    dt_bias [H*dk] -> alpha, same shape as f."""
+    f, A_log, dt_bias = _f64(f), _f64(A_log), _f64(dt_bias)
+    shape = f.shape
+    H, dk = shape[-2], shape[-1]
+    M = int(np.prod(shape[:-2]))
+    assert A_log.shape == (H,) and dt_bias.shape == (H * dk,)
+    alpha = np.empty_like(f)
+    _load().kda_oracle_forget_gate(_p(f), _p(A_log), _p(dt_bias), float(lb), _p(alpha), M, H, dk)
+    return alpha
+
+
+def gated_rmsnorm(o, gate, w, eps=NORM_EPS):
+    """y = o / sqrt(mean(o^2) + eps) * w * sigmoid(gate), per head over dv.
+
+    o, gate [..., H, dv]; w [dv] -> y, same shape as o."""
+    o, gate, w = _f64(o), _f64(gate), _f64(w)
+    shape = o.shape
+    H, dv = shape[-2], shape[-1]
+    M = int(np.prod(shape[:-2]))
+    assert gate.shape == shape and w.shape == (dv,)
+    y = np.empty_like(o)
+    _load().kda_oracle_gated_rmsnorm(_p(o), _p(gate), _p(w), float(eps), _p(y), M, H, dv)
+    return y
+
+
+def decode_step_fused(x, w, cache, f, A_log, dt_bias, beta, S0, scale=1.0,
+                      out_gate=None, norm_w=None, lb=GATE_LOWER_BOUND, eps=L2_EPS,
+                      norm_eps=NORM_EPS):
+    """Decode step with the forget gate in front and, if out_gate is given,
+    the gated RMSNorm behind: alpha = forget_gate(f), then decode_step, then
+    y = gated_rmsnorm(o). Returns (y or o, S, cache)."""
+    alpha = forget_gate(f, A_log, dt_bias, lb)
+    o, S, cache = decode_step(x, w, cache, alpha, beta, S0, scale=scale, eps=eps)
+    if out_gate is not None:
+        o = gated_rmsnorm(o, out_gate, norm_w, norm_eps)
     return o, S, cache
 
 

@@ -169,3 +169,44 @@ void kda_oracle_decode_step(const double *x, const double *w, double *cache,
     free(y);
     free(qkv);
 }
+
+/*
+ * KDA forget gate ([DD] 8.2.3, "The gate in GLM-5.3-Flash, as fla computes
+ * it"): per stream m, head h and key channel c,
+ *     g = lb * sigmoid(exp(A_h) * (f + b_{h,c})),   alpha = exp(g),
+ * with lb the gate's lower bound (-5 in GLM-5.3-Flash).
+ *   f [M][H][dk], A_log [H], dt_bias [H*dk] -> alpha [M][H][dk]
+ */
+void kda_oracle_forget_gate(const double *f, const double *A_log, const double *dt_bias,
+                            double lb, double *alpha, int M, int H, int dk)
+{
+    for (int m = 0; m < M; ++m)
+        for (int h = 0; h < H; ++h)
+            for (int c = 0; c < dk; ++c) {
+                size_t i = ((size_t)m * H + h) * dk + c;
+                double z = exp(A_log[h]) * (f[i] + dt_bias[(size_t)h * dk + c]);
+                double g = lb / (1.0 + exp(-z));
+                alpha[i] = exp(g);
+            }
+}
+
+/*
+ * Gated RMSNorm of one head's output ([DD] 8.2.4 step 7 and its notes:
+ * RMSNorm over the head's dv channels, eps 1e-5, times a sigmoid output gate):
+ *     y_j = o_j / sqrt(mean_j(o^2) + eps) * w_j * sigmoid(gate_j)
+ *   o, gate [M][H][dv], w [dv] -> y [M][H][dv]
+ */
+void kda_oracle_gated_rmsnorm(const double *o, const double *gate, const double *w, double eps,
+                              double *y, int M, int H, int dv)
+{
+    for (int m = 0; m < M; ++m)
+        for (int h = 0; h < H; ++h) {
+            const double *oh = o + ((size_t)m * H + h) * dv;
+            const double *gh = gate + ((size_t)m * H + h) * dv;
+            double *yh = y + ((size_t)m * H + h) * dv;
+            double ss = 0.0;
+            for (int j = 0; j < dv; ++j) ss += oh[j] * oh[j];
+            double r = 1.0 / sqrt(ss / dv + eps);
+            for (int j = 0; j < dv; ++j) yh[j] = oh[j] * r * w[j] / (1.0 + exp(-gh[j]));
+        }
+}

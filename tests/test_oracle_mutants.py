@@ -32,6 +32,16 @@ MUTANTS = {
     "cache_not_shifted": ("c0[c] = c1[c];", "c0[c] = c0[c];"),
 }
 
+GATE_MUTANTS = {
+    "gate_A_not_exponentiated": ("double z = exp(A_log[h]) *", "double z = A_log[h] *"),
+    "gate_bias_dropped": ("(f[i] + dt_bias[(size_t)h * dk + c])", "(f[i])"),
+    "gate_sign": ("double g = lb / (1.0 + exp(-z));", "double g = lb / (1.0 + exp(z));"),
+    "gate_log_space": ("alpha[i] = exp(g);", "alpha[i] = g;"),
+    "norm_sum_not_mean": ("sqrt(ss / dv + eps)", "sqrt(ss + eps)"),
+    "norm_weight_dropped": ("oh[j] * r * w[j] /", "oh[j] * r /"),
+    "norm_gate_not_sigmoid": ("/ (1.0 + exp(-gh[j]))", "* gh[j]"),
+}
+
 PINS = [
     pins.test_worked_example_states,
     pins.test_worked_example_reads,
@@ -47,6 +57,34 @@ PINS = [
     pins.test_conv_identity_weights_is_silu,
     pins.test_conv_matches_direct_causal_convolution,
 ]
+
+
+def _build_mutant(tmp_path, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + old
+    bad = tmp_path / "mutant.c"
+    bad.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", str(bad),
+                           "-o", str(so), "-lm"])
+    return oracle.bind(str(so))
+
+
+@pytest.mark.parametrize("name", sorted(GATE_MUTANTS))
+def test_gate_mutant_is_caught(name, tmp_path, monkeypatch):
+    from tests import test_oracle_gate as gp
+    monkeypatch.setattr(oracle, "_lib", _build_mutant(tmp_path, *GATE_MUTANTS[name]))
+    caught = []
+    for pin in (gp.test_gate_table_keep_factors_and_half_lives, gp.test_gate_neutral_point_and_floor,
+                gp.test_gate_exp_A_scales_the_preactivation, gp.test_gate_bias_per_head_and_channel,
+                gp.test_gate_range, gp.test_norm_constant_vector_and_open_gate,
+                gp.test_norm_scale_invariance_and_unit_rms,
+                gp.test_norm_gate_zero_halves_and_heads_independent):
+        try:
+            pin()
+        except Exception:  # an assertion, or e.g. log of a negative "decay"
+            caught.append(pin.__name__)
+    assert caught, "no pin caught mutant " + name
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
