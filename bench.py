@@ -271,6 +271,51 @@ def time_device(stack: DecodeStack, K: int, W: int, barrier):
     return ev[0].elapsed_time(ev[-1]), step_ms
 
 
+def time_fused(stack: DecodeStack, inputs, K: int, W: int):
+    """The same stack through kda_decode_step_fused: forget gate fused in
+    front (raw gate input f per layer instead of alpha) and gated RMSNorm
+    fused behind (output gate per layer). Graph of L launches, K replays."""
+    torch = stack.torch
+    L, M = stack.L, stack.M
+    dev = stack.x.device
+    gn = inputs.gate_norm_inputs(9, M=M, H=H, T=1)
+    A = torch.from_numpy(gn["A_log"]).to(dev)
+    b = torch.from_numpy(gn["dt_bias"]).to(dev)
+    w = torch.from_numpy(gn["norm_w"]).to(dev)
+    f = torch.from_numpy(gn["f"][0]).to(dev).unsqueeze(0).repeat(L, 1, 1, 1).contiguous()
+    og = torch.from_numpy(gn["out_gate"][0]).to(dev).unsqueeze(0).repeat(L, 1, 1, 1).contiguous()
+    xd = stack.calls[0][0][1]
+    sd = stack.calls[0][0][8]
+    sp = stack.stream.cuda_stream
+    fn = stack.lib.kda_decode_step_fused
+    calls = [(stack.x[l].data_ptr(), xd, stack.conv_w[l].data_ptr(), stack.cache[l].data_ptr(), xd,
+              f[l].data_ptr(), A.data_ptr(), b.data_ptr(), -5.0, stack.beta[l].data_ptr(),
+              stack.state[l].data_ptr(), sd, 1.0, og[l].data_ptr(), w.data_ptr(), 1e-5,
+              stack.o[l].data_ptr(), M, H, DH, DH, sp) for l in range(L)]
+
+    def step():
+        for c in calls:
+            st = fn(*c)
+            if st != 0:
+                raise stack.kda.KdaError("kda_decode_step_fused", st)
+    with torch.cuda.stream(stack.stream):
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stack.stream):
+            step()
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stack.stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stack.stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def time_graph(stack: DecodeStack, K: int, W: int):
     """K replays of one captured CUDA graph holding a whole step (L launches)."""
     torch = stack.torch
@@ -539,6 +584,7 @@ def own_arm(args, rank: int, world: int, local_rank: int):
     sb = state_bytes_per_launch(args.M, args.state_dtype)
     ab = algorithmic_bytes_per_launch(args.M, args.state_dtype, args.x_dtype)
     L = args.layers
+    M_ = args.M
     value = replicas.job_throughput(L * K * sb, world, total_ms * 1e-3) / 1e9
     e2e_value = replicas.job_throughput(L * K * sb, world, e2e_ms * 1e-3) / 1e9
     mean_launch_ms = total_ms / (K * args.layers)   # launch-to-launch, gaps included
@@ -571,6 +617,18 @@ def own_arm(args, rank: int, world: int, local_rank: int):
         "gpu_launches": K * L,
         "clocks": clk,
     }
+    if not args.no_fused:
+        fms = time_fused(stack, inputs, K, 3)
+        fus = fms / K / L * 1e3
+        fab = ab + M_ * H * DH * 4          # + the output gate read (f replaces alpha)
+        line["decode_fused"] = {
+            "workload": "the same stack with the forget gate fused in front (raw gate input "
+                        "instead of alpha) and the gated RMSNorm fused behind",
+            "kernel": "kda_decode_stream_kernel<..., gate, norm>", "us_per_layer": fus,
+            "state_gbs": sb / (fus * 1e-6) / 1e9,
+            "state_frac_of_%s_hbm" % peak_kind: sb / (fus * 1e-6) / 1e9 / peak,
+            "algorithmic_bytes_per_launch": fab,
+            "achieved_gbs": fab / (fus * 1e-6) / 1e9}
     if not args.no_prefill:
         pk = {1: "kda_prefill_simt_kernel", 2: "kda_prefill_tc_kernel"}.get(args.prefill_kernel,
                                                                              "kda_prefill_tc_kernel")
@@ -602,6 +660,8 @@ def main():
                     help="0 auto, 1 cluster (with --columns/--threads), 2 persistent stream")
     ap.add_argument("--columns", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the decode step with the gate and the gated norm fused in")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the chunked-prefill measurement")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor core")

@@ -111,6 +111,32 @@ kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w,
                            void *state, int state_dtype, float scale,
                            float *o, int M, int H, int dk, int dv, void *stream);
 
+/*
+ * kda_decode_step_fused — kda_decode_step with the layer's neighbouring steps
+ * fused in: the KDA forget gate in front and, optionally, the gated RMSNorm
+ * on the output ("GLM-5.3 deep dive", sections 8.2.3 and 8.2.4 step 7).
+ *
+ *   gate_f      [M, H, dk]  FP32 raw forget-gate input f (replaces alpha):
+ *                           alpha = exp(lb * sigmoid(exp(A_log[h]) * (f + dt_bias[h*dk + i])))
+ *   A_log       [H]         FP32
+ *   dt_bias     [H * dk]    FP32
+ *   gate_lower_bound        lb (-5 in GLM-5.3-Flash)
+ *   out_gate    [M, H, dv]  FP32 output-gate input, or NULL for no norm
+ *   norm_weight [dv]        FP32 RMSNorm weight (required with out_gate)
+ *   norm_eps                RMSNorm eps (1e-5 in GLM-5.3-Flash)
+ *   y           [M, H, dv]  FP32 output: o, or with out_gate
+ *                           o / sqrt(mean(o^2) + norm_eps) * norm_weight * sigmoid(out_gate)
+ * All other arguments, layouts and checks as kda_decode_step; y must not
+ * overlap any input or the state.
+ */
+kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w,
+                                 void *conv_cache, int cache_dtype,
+                                 const float *gate_f, const float *A_log, const float *dt_bias,
+                                 float gate_lower_bound, const float *beta,
+                                 void *state, int state_dtype, float scale,
+                                 const float *out_gate, const float *norm_weight, float norm_eps,
+                                 float *y, int M, int H, int dk, int dv, void *stream);
+
 /* Decode kernels selectable through kda_decode_step_config. */
 typedef enum {
     KDA_DECODE_AUTO = 0,    /* the library picks (what kda_decode_step does) */

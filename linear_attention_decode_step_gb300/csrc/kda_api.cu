@@ -131,7 +131,7 @@ kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_
     if (st != KDA_OK) return st;
     const bool explicit_kernel = kernel != KDA_DECODE_AUTO;
     if (!explicit_kernel) kda::default_decode_config(M, H, state_dtype, &kernel, &columns, &threads);
-    kda::DecodeArgs a;
+    kda::DecodeArgs a = {};
     a.x = x;
     a.conv_w = conv_w;
     a.cache = conv_cache;
@@ -205,6 +205,45 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qk
                              void *stream) {
     return kda_chunk_prefill_config(q, k, v, qkv_dtype, alpha, beta, state, o, scale, M, T, H, dk,
                                     dv, chunk, KDA_PREFILL_AUTO, stream);
+}
+
+kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w,
+                                 void *conv_cache, int cache_dtype, const float *gate_f,
+                                 const float *A_log, const float *dt_bias, float gate_lower_bound,
+                                 const float *beta, void *state, int state_dtype, float scale,
+                                 const float *out_gate, const float *norm_weight, float norm_eps,
+                                 float *y, int M, int H, int dk, int dv, void *stream) {
+    if (!A_log || !dt_bias || (out_gate && !norm_weight)) return KDA_ERR_INVALID_ARG;
+    kda_status st = check_decode(x, x_dtype, conv_w, conv_cache, cache_dtype, gate_f, beta, state,
+                                 state_dtype, y, M, H, dk, dv);
+    if (st != KDA_OK) return st;
+    if (!aligned16(A_log) || !aligned16(dt_bias) || (out_gate && !aligned16(out_gate)) ||
+        (norm_weight && !aligned16(norm_weight)))
+        return KDA_ERR_ALIGNMENT;
+    const size_t n_y = (size_t)M * H * dv * sizeof(float);
+    if (overlap(y, n_y, gate_f, (size_t)M * H * dk * sizeof(float)) ||
+        (out_gate && overlap(y, n_y, out_gate, n_y)))
+        return KDA_ERR_INVALID_ARG;
+    kda::DecodeArgs a = {};
+    a.x = x;
+    a.conv_w = conv_w;
+    a.cache = conv_cache;
+    a.alpha = gate_f;
+    a.beta = beta;
+    a.state = state;
+    a.o = y;
+    a.M = M;
+    a.H = H;
+    a.scale = scale;
+    a.l2_prefetch = kda::kDefaultL2Prefetch;
+    a.A_log = A_log;
+    a.dt_bias = dt_bias;
+    a.gate_lb = gate_lower_bound;
+    a.out_gate = out_gate;
+    a.norm_w = norm_weight;
+    a.norm_eps = norm_eps;
+    return cuda_status(kda::launch_decode_stream_fused(a, x_dtype, state_dtype,
+                                                       static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_device_error(void *stream) {

@@ -37,6 +37,13 @@
 //    prefetched into L2 (cp.async.bulk.prefetch.L2).
 //  * Conv weights and beta of a group's next head are prefetched into
 //    registers one head ahead.
+//  * Optional fusions (template flags): the KDA forget gate in front
+//    ("GLM-5.3 deep dive" 8.2.3: alpha = exp(lb sigmoid(e^{A_h} (f + b)))),
+//    computed once per head by 128 threads from the raw gate input f, which
+//    takes alpha's place in the stage (the state is faded after the first
+//    group barrier); and the gated RMSNorm behind (8.2.4 step 7:
+//    y = o / sqrt(mean o^2 + eps) w sigmoid(gate)), applied by the 128 threads
+//    that form o, with one 128-thread barrier for the sum of squares.
 //  * Launched with programmatic stream serialisation: the kernel waits for
 //    the preceding grid (griddepcontrol.wait) before its first global access,
 //    and lets the next launch in the stream start placing CTAs early, which
@@ -88,12 +95,15 @@ struct Cfg {
     static constexpr int X_OFF = A_OFF + DK * 4;
     static constexpr int C_OFF = X_OFF + 3 * DK * (int)sizeof(TX);
     static constexpr int STAGE = C_OFF + 9 * DK * (int)sizeof(TX);
-    // per group: red_u, red_w [CWARPS][DK] | d [DK] | qk [2][DK] | v [DK]
+    // per group: red_u, red_w [CWARPS][DK] | d [DK] | qk [2][DK] | v [DK] |
+    //            alpha from the fused gate [DK] | norm partials [4] (+ pad)
     static constexpr int REDW_F = CWARPS * DK;
     static constexpr int DB_F = 2 * CWARPS * DK;
     static constexpr int QK_F = DB_F + DK;
     static constexpr int V_F = QK_F + 2 * DK;
-    static constexpr int WORK_F = V_F + DK;
+    static constexpr int AB_F = V_F + DK;
+    static constexpr int NRM_F = AB_F + DK;
+    static constexpr int WORK_F = NRM_F + 4;
     static constexpr int WORK_BYTES = WORK_F * 4;
     static constexpr int BAR_BYTES = 2 * 8 * 8;        // full[8], issued[8]
     static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
@@ -183,7 +193,7 @@ __device__ __forceinline__ void load_head(unsigned char *st, uint64_t *bar, cons
                       DK * sizeof(TX), bar);
 }
 
-template <typename TS, typename TX, int G>
+template <typename TS, typename TX, int G, bool GATE, bool NORM>
 __global__ void __launch_bounds__(Cfg<TS, TX, G>::THREADS, 1)
 kda_decode_stream_kernel(const DecodeArgs a) {
     using C = Cfg<TS, TX, G>;
@@ -230,6 +240,8 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     float *db = red + C::DB_F;
     float *qkb = red + C::QK_F;
     float *vb = red + C::V_F;
+    float *ab = red + C::AB_F;
+    float *nrm = red + C::NRM_F;
     TX *cache = static_cast<TX *>(a.cache);
     const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
 
@@ -238,11 +250,21 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     const int c0 = ct, c1 = ct + C::GT;
     float4 wA = make_float4(0.f, 0.f, 0.f, 0.f), wB = wA;
     float beta_n = 0.f;
+    // fused gate: threads GT-128 .. GT-1 own key channel gi; fused norm:
+    // threads 128 .. 255 (the o writers) own value channel ct - 128
+    const int gi = ct - (C::GT - DK);
+    float bias_n = 0.f, eA_n = 0.f, og_n = 0.f;
+    const float nw = (NORM && ct >= DK && ct < 2 * DK) ? __ldg(a.norm_w + ct - DK) : 0.f;
     auto prefetch = [&](int un) {
         const size_t hb = (size_t)(un % H) * DK;
         if (c0 < 3 * DK) wA = __ldg(w4 + (size_t)(c0 / DK) * D + hb + c0 % DK);
         if (c1 < 3 * DK) wB = __ldg(w4 + (size_t)(c1 / DK) * D + hb + c1 % DK);
         beta_n = __ldg(a.beta + un);
+        if (GATE && gi >= 0) {
+            bias_n = __ldg(a.dt_bias + hb + gi);
+            eA_n = __ldg(a.A_log + un % H);
+        }
+        if (NORM && ct >= DK && ct < 2 * DK) og_n = __ldg(a.out_gate + (size_t)un * DK + ct - DK);
     };
 
     int i = g;
@@ -253,6 +275,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         const int m = u / H, h = u - m * H;
         const float4 w0 = wA, w1 = wB;
         const float beta = beta_n;
+        const float bias = bias_n, eA = eA_n, og = og_n;
         const int un = u + G * gridDim.x;
         if (un < n_units) prefetch(un);
 
@@ -275,9 +298,15 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             const int row = p * C::RGROUPS + rg;
             const uint4 r = *reinterpret_cast<const uint4 *>(Ss + row * DK + strip * C::VEC);
             Strip<TS>::unpack(r, sv[p]);
-            const float ar = al[row];
+            if (!GATE) {
+                const float ar = al[row];
 #pragma unroll
-            for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
+                for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
+            }
+        }
+        if (GATE && gi >= 0) {  // alpha = exp(lb sigmoid(e^A (f + b)))
+            const float z = expf(eA) * (al[gi] + bias);
+            ab[gi] = expf(a.gate_lb / (1.0f + expf(-z)));
         }
 
         // (b) conv + SiLU of the head's 384 channels (q, k, v)
@@ -302,6 +331,15 @@ kda_decode_stream_kernel(const DecodeArgs a) {
                 ptx::mbar_arrive(&issued[s]);
                 const int up = ur + P * gridDim.x;
                 if (P > 0 && up < n_units) prefetch_head<TS>(a, up);
+            }
+        }
+
+        if (GATE) {  // fade now that the gate's alpha is in shared memory
+#pragma unroll
+            for (int p = 0; p < C::RPT; ++p) {
+                const float ar = ab[p * C::RGROUPS + rg];
+#pragma unroll
+                for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
             }
         }
 
@@ -366,8 +404,19 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             for (int q = 0; q < C::CWARPS; ++q) wt += redw[q * DK + ct - DK];
         }
         ptx::named_bar_sync(bar_id, C::GT);  // barrier 3: d published
-        if (ct >= DK && ct < 2 * DK)  // o_j = scale (w_j + d_j (k.q))
-            a.o[(size_t)u * DK + ct - DK] = a.scale * fmaf(db[ct - DK], kq, wt);
+        if (ct >= DK && ct < 2 * DK) {  // o_j = scale (w_j + d_j (k.q))
+            float oj = a.scale * fmaf(db[ct - DK], kq, wt);
+            if (NORM) {  // y_j = o_j / sqrt(mean o^2 + eps) * w_j * sigmoid(gate_j)
+                float ss = oj * oj;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (lane == 0) nrm[(ct - DK) >> 5] = ss;
+                ptx::named_bar_sync(3 + g, DK);
+                ss = nrm[0] + nrm[1] + nrm[2] + nrm[3];
+                oj = oj * (1.0f / sqrtf(ss * (1.0f / DK) + a.norm_eps)) * nw / (1.0f + expf(-og));
+            }
+            a.o[(size_t)u * DK + ct - DK] = oj;
+        }
 
         // (f) S' = s + k d, streamed out with 128-bit stores
         float dd[C::VEC];
@@ -391,16 +440,16 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     }
 }
 
-template <typename TS, typename TX, int G>
+template <typename TS, typename TX, int G, bool GATE, bool NORM>
 cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
     using C = Cfg<TS, TX, G>;
+    auto kernel = kda_decode_stream_kernel<TS, TX, G, GATE, NORM>;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_decode_stream_kernel<TS, TX, G>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const int units = a.M * a.H;
     const int grid = units < sms ? units : sms;
@@ -414,14 +463,20 @@ cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kda_decode_stream_kernel<TS, TX, G>, a);
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <typename TS, typename TX>
 cudaError_t launch_groups(const DecodeArgs &a, int groups, cudaStream_t stream) {
-    if (groups == 1) return launch_stream_typed<TS, TX, 1>(a, stream);
-    if (groups == 2) return launch_stream_typed<TS, TX, 2>(a, stream);
+    if (groups == 1) return launch_stream_typed<TS, TX, 1, false, false>(a, stream);
+    if (groups == 2) return launch_stream_typed<TS, TX, 2, false, false>(a, stream);
     return cudaErrorNotSupported;
+}
+
+template <typename TS, typename TX>
+cudaError_t launch_fused(const DecodeArgs &a, cudaStream_t stream) {
+    if (a.out_gate) return launch_stream_typed<TS, TX, 2, true, true>(a, stream);
+    return launch_stream_typed<TS, TX, 2, true, false>(a, stream);
 }
 
 }  // namespace
@@ -433,6 +488,15 @@ cudaError_t launch_decode_stream(const DecodeArgs &a, int x_dtype, int state_dty
     if (sb) return launch_groups<__nv_bfloat16, float>(a, groups, stream);
     if (xb) return launch_groups<float, __nv_bfloat16>(a, groups, stream);
     return launch_groups<float, float>(a, groups, stream);
+}
+
+cudaError_t launch_decode_stream_fused(const DecodeArgs &a, int x_dtype, int state_dtype,
+                                       cudaStream_t stream) {
+    const bool xb = x_dtype == KDA_BF16, sb = state_dtype == KDA_BF16;
+    if (sb && xb) return launch_fused<__nv_bfloat16, __nv_bfloat16>(a, stream);
+    if (sb) return launch_fused<__nv_bfloat16, float>(a, stream);
+    if (xb) return launch_fused<float, __nv_bfloat16>(a, stream);
+    return launch_fused<float, float>(a, stream);
 }
 
 cudaError_t take_stream_error(unsigned int *code) {

@@ -24,6 +24,14 @@ struct DecodeArgs {
     int M, H;
     float scale;
     int l2_prefetch;       // streaming kernel: heads prefetched into L2 beyond the ring
+    // fused forget gate: alpha holds the raw gate input f; alpha = exp(lb sigmoid(e^A (f + b)))
+    const float *A_log;    // [H]
+    const float *dt_bias;  // [H*128]
+    float gate_lb;
+    // fused gated RMSNorm on o: y = o / sqrt(mean o^2 + eps) * w * sigmoid(out_gate)
+    const float *out_gate; // [M, H, 128]
+    const float *norm_w;   // [128]
+    float norm_eps;
 };
 
 // Arguments of one chunked prefill (layouts as documented in kda.h).
@@ -56,6 +64,11 @@ cudaError_t launch_decode(const DecodeArgs &a, int x_dtype, int state_dtype,
 // `groups` = 1 or 2 consumer groups). cudaErrorNotSupported for other groups.
 cudaError_t launch_decode_stream(const DecodeArgs &a, int x_dtype, int state_dtype, int groups,
                                  cudaStream_t stream);
+
+// Streaming decode kernel with the forget gate fused in front (a.alpha is the
+// raw gate input) and, if a.out_gate is set, the gated RMSNorm fused behind.
+cudaError_t launch_decode_stream_fused(const DecodeArgs &a, int x_dtype, int state_dtype,
+                                       cudaStream_t stream);
 
 // Picks the decode kernel (KDA_DECODE_CLUSTER or KDA_DECODE_STREAM) and, for
 // the cluster kernel, its work split (columns per CTA, threads per CTA).

@@ -34,6 +34,7 @@ __all__ = [
     "decode_layer",
     "prefill_problem",
     "layer_seed",
+    "gate_norm_inputs",
 ]
 
 
@@ -126,3 +127,20 @@ def prefill_problem(seed: int, M: int, T: int, H: int = 64, d: int = 128,
     out["beta"] = _sigmoid32(rng.standard_normal((M, T, H)))
     out["alpha"] = _sigmoid32(rng.standard_normal((M, T, H, d), dtype=np.float32) + alpha_mean)
     return out
+
+
+def gate_norm_inputs(seed: int, M: int, H: int = 64, d: int = 128, T: int = 1) -> dict:
+    """Inputs of the steps fused around the decode step: the forget gate's raw
+    input f ~ N(0, 1) [M, H, d] per step, A_log ~ U(-1, 1) [H], dt_bias ~
+    N(0, 1) [H*d]; the output gate's input ~ N(0, 1) [M, H, d] per step and
+    the RMSNorm weight ~ N(1, 0.1^2) [d]. All FP32. Draw order: A_log,
+    dt_bias, norm_w, then per step (f, out_gate)."""
+    rng = np.random.default_rng(seed)
+    A_log = rng.uniform(-1.0, 1.0, H).astype(np.float32)
+    dt_bias = rng.standard_normal(H * d).astype(np.float32)
+    norm_w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    f, og = [], []
+    for _ in range(T):
+        f.append(rng.standard_normal((M, H, d)).astype(np.float32))
+        og.append(rng.standard_normal((M, H, d)).astype(np.float32))
+    return {"A_log": A_log, "dt_bias": dt_bias, "norm_w": norm_w, "f": f, "out_gate": og}

@@ -27,6 +27,7 @@ __all__ = [
     "KdaError", "lib", "library_path", "header_functions",
     "kda_status_string", "kda_last_cuda_error", "kda_version",
     "kda_conv_step", "kda_decode_step", "kda_decode_step_config", "kda_device_error",
+    "kda_decode_step_fused",
 ]
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2
@@ -53,6 +54,8 @@ _SIGNATURES = {
     "kda_decode_step_config": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
                                 _I, _I, _I, _I, _I, _I, _I, _V], _I),
     "kda_device_error": ([_V], _I),
+    "kda_decode_step_fused": ([_V, _I, _V, _V, _I, _V, _V, _V, _F, _V, _V, _I, _F, _V, _V, _F, _V,
+                               _I, _I, _I, _I, _V], _I),
     "kda_chunk_prefill": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I, _V], _I),
     "kda_chunk_prefill_config": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I,
                                   _I, _V], _I),
@@ -192,6 +195,24 @@ def kda_decode_step_config(x, conv_w, conv_cache, alpha, beta, state, o=None, sc
                                       _stream(stream))
     _check("kda_decode_step_config", st)
     return o
+
+
+def kda_decode_step_fused(x, conv_w, conv_cache, gate_f, A_log, dt_bias, beta, state, y=None,
+                          scale=1.0, gate_lower_bound=-5.0, out_gate=None, norm_weight=None,
+                          norm_eps=1e-5, stream=None):
+    """Decode step with the forget gate fused in front (gate_f replaces alpha)
+    and, with out_gate and norm_weight, the gated RMSNorm fused behind.
+    Returns y [M,H,128] f32."""
+    M, H, dk, dv, y, args = _decode_args(x, conv_w, conv_cache, gate_f, beta, state, y)
+    og = _dev(out_gate, "out_gate", torch.float32) if out_gate is not None else None
+    nw = _dev(norm_weight, "norm_weight", torch.float32) if norm_weight is not None else None
+    st = lib().kda_decode_step_fused(
+        args[0], args[1], args[2], args[3], args[4], args[5],
+        _dev(A_log, "A_log", torch.float32), _dev(dt_bias, "dt_bias", torch.float32),
+        float(gate_lower_bound), args[6], args[7], args[8], float(scale), og, nw, float(norm_eps),
+        _dev(y, "y", torch.float32), M, H, dk, dv, _stream(stream))
+    _check("kda_decode_step_fused", st)
+    return y
 
 
 def kda_device_error(stream=None) -> int:
