@@ -39,9 +39,9 @@
 //    registers one head ahead.
 //  * Optional fusions (template flags): the KDA forget gate in front
 //    ("GLM-5.3 deep dive" 8.2.3: alpha = exp(lb sigmoid(e^{A_h} (f + b)))),
-//    computed once per head by 128 threads from the raw gate input f, which
-//    takes alpha's place in the stage (the state is faded after the first
-//    group barrier); and the gated RMSNorm behind (8.2.4 step 7:
+//    computed by 128 threads of a group one head ahead (while the group
+//    reduces the current head) into a double-buffered shared array, so the
+//    fade stays on the load path; and the gated RMSNorm behind (8.2.4 step 7:
 //    y = o / sqrt(mean o^2 + eps) w sigmoid(gate)), applied by the 128 threads
 //    that form o, with one 128-thread barrier for the sum of squares.
 //  * Launched with programmatic stream serialisation: the kernel waits for
@@ -101,8 +101,8 @@ struct Cfg {
     static constexpr int DB_F = 2 * CWARPS * DK;
     static constexpr int QK_F = DB_F + DK;
     static constexpr int V_F = QK_F + 2 * DK;
-    static constexpr int AB_F = V_F + DK;
-    static constexpr int NRM_F = AB_F + DK;
+    static constexpr int AB_F = V_F + DK;      // [2][DK]: alpha of this head and the next
+    static constexpr int NRM_F = AB_F + 2 * DK;
     static constexpr int WORK_F = NRM_F + 4;
     static constexpr int WORK_BYTES = WORK_F * 4;
     static constexpr int BAR_BYTES = 2 * 8 * 8;        // full[8], issued[8]
@@ -169,8 +169,9 @@ __device__ __forceinline__ void prefetch_head(const DecodeArgs &a, int u) {
                           DK * DK * sizeof(TS));
 }
 
-// Issues the bulk copies of head u into stage `st`, completing on `bar`.
-template <typename TS, typename TX, int G>
+// Issues the bulk copies of head u into stage `st`, completing on `bar`
+// (without alpha when the fused gate computes it).
+template <typename TS, typename TX, int G, bool GATE>
 __device__ __forceinline__ void load_head(unsigned char *st, uint64_t *bar, const DecodeArgs &a,
                                           int u, uint64_t pol) {
     using C = Cfg<TS, TX, G>;
@@ -179,10 +180,10 @@ __device__ __forceinline__ void load_head(unsigned char *st, uint64_t *bar, cons
     const int m = u / H, h = u - m * H;
     const TX *x = static_cast<const TX *>(a.x);
     const TX *cache = static_cast<const TX *>(a.cache);
-    ptx::mbar_arrive_expect_tx(bar, C::STAGE);
+    ptx::mbar_arrive_expect_tx(bar, GATE ? C::STAGE - DK * 4 : C::STAGE);
     ptx::bulk_g2s_hint(st, static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES, bar,
                        pol);
-    ptx::bulk_g2s(st + C::A_OFF, a.alpha + (size_t)u * DK, DK * 4, bar);
+    if (!GATE) ptx::bulk_g2s(st + C::A_OFF, a.alpha + (size_t)u * DK, DK * 4, bar);
 #pragma unroll
     for (int X = 0; X < 3; ++X)
         ptx::bulk_g2s(st + C::X_OFF + X * DK * sizeof(TX), x + ((size_t)m * 3 + X) * D + (size_t)h * DK,
@@ -221,7 +222,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
             const int u = blockIdx.x + s * gridDim.x;
-            if (u < n_units) load_head<TS, TX, G>(smem + s * C::STAGE, &full[s], a, u, pol);
+            if (u < n_units) load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, u, pol);
         }
         for (int j = 0; j < P; ++j) {
             const int u = blockIdx.x + (C::NST + j) * gridDim.x;
@@ -253,7 +254,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     // fused gate: threads GT-128 .. GT-1 own key channel gi; fused norm:
     // threads 128 .. 255 (the o writers) own value channel ct - 128
     const int gi = ct - (C::GT - DK);
-    float bias_n = 0.f, eA_n = 0.f, og_n = 0.f;
+    float bias_n = 0.f, eA_n = 0.f, f_n = 0.f, og_n = 0.f;
     const float nw = (NORM && ct >= DK && ct < 2 * DK) ? __ldg(a.norm_w + ct - DK) : 0.f;
     auto prefetch = [&](int un) {
         const size_t hb = (size_t)(un % H) * DK;
@@ -263,19 +264,31 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         if (GATE && gi >= 0) {
             bias_n = __ldg(a.dt_bias + hb + gi);
             eA_n = __ldg(a.A_log + un % H);
+            f_n = __ldg(a.alpha + (size_t)un * DK + gi);
         }
         if (NORM && ct >= DK && ct < 2 * DK) og_n = __ldg(a.out_gate + (size_t)un * DK + ct - DK);
+    };
+
+    // alpha = exp(lb sigmoid(e^A (f + b))) of the prefetched head, into ab[buf]
+    auto gate = [&](int buf) {
+        const float z = __expf(eA_n) * (f_n + bias_n);
+        ab[buf * DK + gi] = __expf(a.gate_lb / (1.0f + __expf(-z)));
     };
 
     int i = g;
     int u = blockIdx.x + i * gridDim.x;
     if (u < n_units) prefetch(u);
+    if (GATE) {  // the group's first head; later heads are gated one iteration ahead
+        if (u < n_units && gi >= 0) gate(0);
+        __syncthreads();
+    }
     for (; u < n_units; i += G, u += G * gridDim.x) {
         const int s = i % C::NST, n = i / C::NST;
         const int m = u / H, h = u - m * H;
         const float4 w0 = wA, w1 = wB;
         const float beta = beta_n;
-        const float bias = bias_n, eA = eA_n, og = og_n;
+        const float og = og_n;
+        const int ib = (i / G) & 1;  // this head's alpha buffer (fused gate)
         const int un = u + G * gridDim.x;
         if (un < n_units) prefetch(un);
 
@@ -298,15 +311,9 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             const int row = p * C::RGROUPS + rg;
             const uint4 r = *reinterpret_cast<const uint4 *>(Ss + row * DK + strip * C::VEC);
             Strip<TS>::unpack(r, sv[p]);
-            if (!GATE) {
-                const float ar = al[row];
+            const float ar = GATE ? ab[ib * DK + row] : al[row];
 #pragma unroll
-                for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
-            }
-        }
-        if (GATE && gi >= 0) {  // alpha = exp(lb sigmoid(e^A (f + b)))
-            const float z = expf(eA) * (al[gi] + bias);
-            ab[gi] = expf(a.gate_lb / (1.0f + expf(-z)));
+            for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
         }
 
         // (b) conv + SiLU of the head's 384 channels (q, k, v)
@@ -327,21 +334,16 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         if (ct == 0) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;  // refill with head i + NST
             if (ur < n_units) {
-                load_head<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, ur, pol);
                 ptx::mbar_arrive(&issued[s]);
                 const int up = ur + P * gridDim.x;
                 if (P > 0 && up < n_units) prefetch_head<TS>(a, up);
             }
         }
 
-        if (GATE) {  // fade now that the gate's alpha is in shared memory
-#pragma unroll
-            for (int p = 0; p < C::RPT; ++p) {
-                const float ar = ab[p * C::RGROUPS + rg];
-#pragma unroll
-                for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
-            }
-        }
+        // fused gate: alpha of the group's next head (its inputs were
+        // prefetched at the top of this iteration), visible after barrier 2
+        if (GATE && gi >= 0 && un < n_units) gate(ib ^ 1);
 
         // (c) norms, formed by every warp from shared memory (lane: 4 channels)
         const float4 q4 = reinterpret_cast<const float4 *>(qkb)[lane];
@@ -413,7 +415,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
                 if (lane == 0) nrm[(ct - DK) >> 5] = ss;
                 ptx::named_bar_sync(3 + g, DK);
                 ss = nrm[0] + nrm[1] + nrm[2] + nrm[3];
-                oj = oj * (1.0f / sqrtf(ss * (1.0f / DK) + a.norm_eps)) * nw / (1.0f + expf(-og));
+                oj = oj * rsqrtf(ss * (1.0f / DK) + a.norm_eps) * nw / (1.0f + __expf(-og));
             }
             a.o[(size_t)u * DK + ct - DK] = oj;
         }
