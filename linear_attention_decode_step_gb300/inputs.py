@@ -35,6 +35,7 @@ __all__ = [
     "prefill_problem",
     "layer_seed",
     "gate_norm_inputs",
+    "stack_tokens",
 ]
 
 
@@ -144,3 +145,16 @@ def gate_norm_inputs(seed: int, M: int, H: int = 64, d: int = 128, T: int = 1) -
         f.append(rng.standard_normal((M, H, d)).astype(np.float32))
         og.append(rng.standard_normal((M, H, d)).astype(np.float32))
     return {"A_log": A_log, "dt_bias": dt_bias, "norm_w": norm_w, "f": f, "out_gate": og}
+
+
+def stack_tokens(layer: dict) -> dict:
+    """The T steps of a ``decode_layer`` dict as token-major arrays for a
+    multi-token call: x_bits uint16 [M, T, 3, D] (x_f32 widened), alpha
+    float32 [M, T, H, d], beta float32 [M, T, H]."""
+    x_bits = np.ascontiguousarray(np.stack(layer["x_bits"], axis=1))
+    return {
+        "x_bits": x_bits,
+        "x_f32": bf16_widen(x_bits),
+        "alpha": np.ascontiguousarray(np.stack(layer["alpha"], axis=1)),
+        "beta": np.ascontiguousarray(np.stack(layer["beta"], axis=1)),
+    }

@@ -36,6 +36,7 @@ __all__ = [
     "forget_gate",
     "gated_rmsnorm",
     "decode_step_fused",
+    "decode_tokens",
     "L2_EPS",
     "GATE_LOWER_BOUND",
     "NORM_EPS",
@@ -190,6 +191,26 @@ def decode_step_fused(x, w, cache, f, A_log, dt_bias, beta, S0, scale=1.0,
     if out_gate is not None:
         o = gated_rmsnorm(o, out_gate, norm_w, norm_eps)
     return o, S, cache
+
+
+def decode_tokens(x, w, cache, alpha, beta, S0, scale=1.0, eps=L2_EPS):
+    """T consecutive decode steps of one KDA layer in one call (the
+    fused-recurrent mode of "GLM-5.3 deep dive" 8.2.5, used when a few tokens
+    arrive at once, e.g. to verify drafted tokens): the decode step above,
+    applied to tokens t = 0 .. T-1 in order, each one seeing the conv cache
+    and the state the previous one left.
+
+    x [M,T,3,D]; w [3,D,4]; cache [M,3,3,D]; alpha [M,T,H,d]; beta [M,T,H];
+    S0 [M,H,d,d] -> (o [M,T,H,d], S [M,H,d,d], cache [M,3,3,D]).
+    """
+    x, alpha, beta = _f64(x), _f64(alpha), _f64(beta)
+    M, T = x.shape[:2]
+    S, c = _f64(S0), _f64(cache)
+    o = np.empty(alpha.shape[:3] + (S.shape[-1],), dtype=np.float64)
+    for t in range(T):
+        o[:, t], S, c = decode_step(x[:, t], w, c, alpha[:, t], beta[:, t], S,
+                                    scale=scale, eps=eps)
+    return o, S, c
 
 
 def _l2norm_rows(x, eps):

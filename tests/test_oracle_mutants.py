@@ -105,3 +105,31 @@ def test_mutant_is_caught(name, tmp_path, monkeypatch):
         except AssertionError:
             caught.append(getattr(pin, "__name__", "pin"))
     assert caught, "no pin caught mutant " + name
+
+
+def _tokens_variant(kind):
+    """A copy of oracle.decode_tokens with one planted mistake."""
+    import numpy as np
+
+    def run(x, w, cache, alpha, beta, S0, scale=1.0, eps=oracle.L2_EPS):
+        T = x.shape[1]
+        S, c = np.array(S0, dtype=np.float64), np.array(cache, dtype=np.float64)
+        o = np.empty(alpha.shape[:3] + (S.shape[-1],))
+        order = range(T - 1, -1, -1) if kind == "reversed" else range(T)
+        for t in order:
+            ta = 0 if kind == "alpha_of_first" else t
+            c_in = cache if kind == "cache_not_carried" else c
+            S_in = S0 if kind == "state_not_carried" else S
+            o[:, t], S, c = oracle.decode_step(x[:, t], w, c_in, alpha[:, ta], beta[:, t], S_in,
+                                               scale=scale, eps=eps)
+        return o, S, c
+    return run
+
+
+@pytest.mark.parametrize("kind", ["alpha_of_first", "cache_not_carried", "state_not_carried",
+                                  "reversed"])
+def test_tokens_mutant_is_caught(kind, monkeypatch):
+    from tests import test_oracle_tokens as tp
+    monkeypatch.setattr(oracle, "decode_tokens", _tokens_variant(kind))
+    with pytest.raises(AssertionError):
+        tp.test_tokens_equal_convolution_then_chunked_form(5)
