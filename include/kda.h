@@ -137,6 +137,34 @@ kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w
                                  const float *out_gate, const float *norm_weight, float norm_eps,
                                  float *y, int M, int H, int dk, int dv, void *stream);
 
+/*
+ * kda_decode_tokens — T consecutive decode steps of one KDA layer for M
+ * streams in one launch: token t = 0 .. T-1 goes through exactly the steps of
+ * kda_decode_step, seeing the conv cache and state the previous token left
+ * (the fused-recurrent mode of "GLM-5.3 deep dive" section 8.2.5, for a few
+ * tokens at once, e.g. verifying drafted tokens). Each head's state and conv
+ * cache are read from HBM once and written once per call.
+ *
+ *   x           [M, T, 3, H*dk] pre-conv q, k, v of the T tokens (x_dtype)
+ *   conv_w      [3, H*dk, 4]    as kda_decode_step
+ *   conv_cache  [M, 3, 3, H*dk] in place; afterwards it holds the last three
+ *                               inputs of the sequence (cache, x_0 .. x_{T-1})
+ *   alpha       [M, T, H, dk]   FP32 per-token decay, linear space
+ *   beta        [M, T, H]       FP32
+ *   state       [M, H, dk, dv]  in place. The state stays FP32 across the T
+ *                               tokens; with BF16 storage it is rounded once,
+ *                               when stored at the end of the call.
+ *   o           [M, T, H, dv]   FP32 outputs of every token
+ *   T >= 1 (state traffic is amortised over T; the arithmetic grows with T,
+ *   so for long inputs the chunked prefill is the faster path).
+ * Other arguments, checks and errors as kda_decode_step (sizes scale with T).
+ */
+kda_status kda_decode_tokens(const void *x, int x_dtype, const float *conv_w,
+                             void *conv_cache, int cache_dtype,
+                             const float *alpha, const float *beta,
+                             void *state, int state_dtype, float scale,
+                             float *o, int M, int T, int H, int dk, int dv, void *stream);
+
 /* Decode kernels selectable through kda_decode_step_config. */
 typedef enum {
     KDA_DECODE_AUTO = 0,    /* the library picks (what kda_decode_step does) */

@@ -35,10 +35,10 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb) {
 
 kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
                         int cache_dtype, const float *alpha, const float *beta, void *state,
-                        int state_dtype, float *o, int M, int H, int dk, int dv) {
+                        int state_dtype, float *o, int M, int H, int dk, int dv, int T = 1) {
     if (!x || !conv_w || !conv_cache || !alpha || !beta || !state || !o)
         return KDA_ERR_INVALID_ARG;
-    if (M <= 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+    if (M <= 0 || H <= 0 || dk <= 0 || dv <= 0 || T <= 0) return KDA_ERR_INVALID_ARG;
     if (!valid_dtype(x_dtype) || !valid_dtype(cache_dtype) || !valid_dtype(state_dtype))
         return KDA_ERR_INVALID_ARG;
     if (dk != kda::kHeadDim || dv != kda::kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -49,9 +49,9 @@ kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *c
         return KDA_ERR_ALIGNMENT;
     const size_t D = (size_t)H * dk;
     const size_t n_state = (size_t)M * H * dk * dv * dtype_bytes(state_dtype);
-    const size_t n_o = (size_t)M * H * dv * sizeof(float);
+    const size_t n_o = (size_t)M * T * H * dv * sizeof(float);
     const size_t n_cache = (size_t)M * 9 * D * dtype_bytes(cache_dtype);
-    const size_t n_x = (size_t)M * 3 * D * dtype_bytes(x_dtype);
+    const size_t n_x = (size_t)M * T * 3 * D * dtype_bytes(x_dtype);
     if (overlap(o, n_o, state, n_state) || overlap(o, n_o, conv_cache, n_cache) ||
         overlap(o, n_o, x, n_x) || overlap(state, n_state, conv_cache, n_cache))
         return KDA_ERR_INVALID_ARG;
@@ -244,6 +244,28 @@ kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w
     a.norm_eps = norm_eps;
     return cuda_status(kda::launch_decode_stream_fused(a, x_dtype, state_dtype,
                                                        static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_decode_tokens(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
+                             int cache_dtype, const float *alpha, const float *beta, void *state,
+                             int state_dtype, float scale, float *o, int M, int T, int H, int dk,
+                             int dv, void *stream) {
+    const kda_status st = check_decode(x, x_dtype, conv_w, conv_cache, cache_dtype, alpha, beta,
+                                       state, state_dtype, o, M, H, dk, dv, T);
+    if (st != KDA_OK) return st;
+    kda::DecodeArgs a = {};
+    a.x = x;
+    a.conv_w = conv_w;
+    a.cache = conv_cache;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.state = state;
+    a.o = o;
+    a.M = M;
+    a.H = H;
+    a.scale = scale;
+    return cuda_status(kda::launch_decode_tokens(a, T, x_dtype, state_dtype,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_device_error(void *stream) {

@@ -70,6 +70,12 @@ cudaError_t launch_decode_stream(const DecodeArgs &a, int x_dtype, int state_dty
 cudaError_t launch_decode_stream_fused(const DecodeArgs &a, int x_dtype, int state_dtype,
                                        cudaStream_t stream);
 
+// T consecutive decode steps in one launch (x [M, T, 3, H*128], alpha
+// [M, T, H, 128], beta [M, T, H], o [M, T, H, 128]; state and conv cache read
+// once and written once).
+cudaError_t launch_decode_tokens(const DecodeArgs &a, int T, int x_dtype, int state_dtype,
+                                 cudaStream_t stream);
+
 // Picks the decode kernel (KDA_DECODE_CLUSTER or KDA_DECODE_STREAM) and, for
 // the cluster kernel, its work split (columns per CTA, threads per CTA).
 void default_decode_config(int M, int H, int state_dtype, int *kernel, int *columns,

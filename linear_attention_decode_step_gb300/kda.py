@@ -56,6 +56,8 @@ _SIGNATURES = {
     "kda_device_error": ([_V], _I),
     "kda_decode_step_fused": ([_V, _I, _V, _V, _I, _V, _V, _V, _F, _V, _V, _I, _F, _V, _V, _F, _V,
                                _I, _I, _I, _I, _V], _I),
+    "kda_decode_tokens": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
+                           _I, _I, _I, _I, _I, _V], _I),
     "kda_chunk_prefill": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I, _V], _I),
     "kda_chunk_prefill_config": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I,
                                   _I, _V], _I),
@@ -213,6 +215,26 @@ def kda_decode_step_fused(x, conv_w, conv_cache, gate_f, A_log, dt_bias, beta, s
         _dev(y, "y", torch.float32), M, H, dk, dv, _stream(stream))
     _check("kda_decode_step_fused", st)
     return y
+
+
+def kda_decode_tokens(x, conv_w, conv_cache, alpha, beta, state, o=None, scale=1.0,
+                      stream=None):
+    """T consecutive decode steps in one call (see kda.h). x [M,T,3,H*128]
+    (bf16|f32, pre-conv), alpha [M,T,H,128] f32, beta [M,T,H] f32; state
+    [M,H,128,128] (f32|bf16) and conv_cache are updated in place; returns
+    o [M,T,H,128] f32."""
+    M, H, dk, dv = state.shape
+    T = x.shape[1]
+    if o is None:
+        o = torch.empty((M, T, H, dv), dtype=torch.float32, device=state.device)
+    st = lib().kda_decode_tokens(
+        _dev(x, "x"), _dtype_code(x), _dev(conv_w, "conv_w", torch.float32),
+        _dev(conv_cache, "conv_cache"), _dtype_code(conv_cache),
+        _dev(alpha, "alpha", torch.float32), _dev(beta, "beta", torch.float32),
+        _dev(state, "state"), _dtype_code(state), float(scale), _dev(o, "o", torch.float32),
+        M, T, H, dk, dv, _stream(stream))
+    _check("kda_decode_tokens", st)
+    return o
 
 
 def kda_device_error(stream=None) -> int:

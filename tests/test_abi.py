@@ -138,3 +138,23 @@ def _prefill_call(K, **over):
 ])
 def test_prefill_rejects(K, over, status):
     assert _prefill_call(K, **over) == status
+
+
+def _tokens_call(K, **over):
+    a = dict(x=BASE, xd=K.KDA_BF16, w=BASE + GAP, cache=BASE + 2 * GAP, cd=K.KDA_BF16,
+             alpha=BASE + 3 * GAP, beta=BASE + 4 * GAP, state=BASE + 5 * GAP,
+             sd=K.KDA_F32, scale=1.0, o=BASE + 6 * GAP, M=4, T=8, H=64, dk=128, dv=128)
+    a.update(over)
+    return K.lib().kda_decode_tokens(a["x"], a["xd"], a["w"], a["cache"], a["cd"], a["alpha"],
+                                     a["beta"], a["state"], a["sd"], a["scale"], a["o"],
+                                     a["M"], a["T"], a["H"], a["dk"], a["dv"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(T=0), 1), (dict(T=-1), 1), (dict(x=None), 1), (dict(o=None), 1),
+    (dict(M=0), 1), (dict(dk=64), 2), (dict(cd=0), 2), (dict(alpha=BASE + 3 * GAP + 8), 3),
+    # o spans M*T*H*128 floats: its end (4*8*64*128*4 bytes = 1 MiB) reaches the state
+    (dict(o=BASE + 5 * GAP - (1 << 20) + 16), 1),
+])
+def test_tokens_rejects(K, over, status):
+    assert _tokens_call(K, **over) == status
