@@ -483,6 +483,67 @@ def prefill_summary(ms, M, T, peak_hbm, peak_bf16, kernel_name):
     }
 
 
+SM_COUNT = 152          # GB300
+FP32_LANES_PER_SM = 128
+MAX_SM_MHZ = 2070.0
+
+
+def fp32_peak_tflops(sm_mhz=None):
+    """FP32 FMA peak derived from the unit counts: 152 SMs x 128 lanes x
+    2 flop per FMA x the SM clock (the sampled median under load, else the
+    2070 MHz maximum)."""
+    mhz = sm_mhz if sm_mhz else MAX_SM_MHZ
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def time_tokens(torch, kda, inputs, M, T, state_dtype, K, W):
+    """K multi-token decode calls (T tokens each) of one layer at M streams x
+    64 heads, alternating between two state buffers (together larger than L2).
+    Returns ms per call."""
+    inp = inputs.decode_layer(inputs.layer_seed(5, T), M=M, H=H, T=T)
+    tok = inputs.stack_tokens(inp)
+    dev = torch.device("cuda")
+    bf = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    x, cache = bf(tok["x_bits"]), bf(inp["cache_bits"])
+    w = torch.from_numpy(inp["conv_w"]).to(dev)
+    alpha = torch.from_numpy(tok["alpha"]).to(dev)
+    beta = torch.from_numpy(tok["beta"]).to(dev)
+    S0 = torch.from_numpy(inp["S0"]).to(dev)
+    Ss = [S0.to(torch.bfloat16) if state_dtype == "bf16" else S0.clone() for _ in range(2)]
+    o = torch.empty((M, T, H, DH), dtype=torch.float32, device=dev)
+    del inp, tok
+    run = lambda i: kda.kda_decode_tokens(x, w, cache, alpha, beta, Ss[i & 1], o)
+    for i in range(W):
+        run(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        run(i)
+    e1.record()
+    torch.cuda.synchronize()
+    if kda.kda_device_error() != kda.KDA_OK:
+        raise RuntimeError("multi-token decode reported a device-side timeout")
+    return e0.elapsed_time(e1) / K
+
+
+def tokens_summary(ms, M, T, state_dtype, peak_hbm, sm_mhz):
+    """Roofline of one multi-token call: the state is read and written once
+    (HBM), each token costs 7 dk dv flops per head on CUDA cores (fade,
+    two column sums, rank-1 correction)."""
+    us = ms * 1e3
+    sb = state_bytes_per_launch(M, state_dtype)
+    flops = 7 * DH * DH * M * H * T
+    fp32 = fp32_peak_tflops(sm_mhz)
+    t_hbm = sb / (peak_hbm * 1e9) * 1e6
+    t_alu = flops / (fp32 * 1e12) * 1e6
+    return {"T": T, "us_per_call": us, "us_per_token": us / T,
+            "state_gbs": sb / (us * 1e-6) / 1e9,
+            "tflop_s": flops / (us * 1e-6) / 1e12,
+            "bound": "hbm" if t_hbm >= t_alu else "alu",
+            "roofline_us": max(t_hbm, t_alu), "frac_of_roofline": max(t_hbm, t_alu) / us}
+
+
 def measured_bf16():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -635,6 +696,18 @@ def own_arm(args, rank: int, world: int, local_rank: int):
         pms = time_prefill(torch, kda, inputs, 4, 4096, min(args.steps, 20), 3,
                            kernel=args.prefill_kernel)
         line["prefill"] = prefill_summary(pms, 4, 4096, peak, measured_bf16(), pk)
+    if not args.no_tokens:
+        mhz = clk.get("sm_mhz") if isinstance(clk, dict) else None
+        rows = [tokens_summary(time_tokens(torch, kda, inputs, M_, T, args.state_dtype, 30, 3),
+                               M_, T, args.state_dtype, peak, mhz) for T in (2, 4, 8)]
+        line["decode_tokens"] = {
+            "workload": "multi-token decode (kda_decode_tokens): one layer, M=%d streams x 64 "
+                        "heads, T tokens per call, %s state, BF16 q/k/v" % (M_, args.state_dtype),
+            "kernel": "kda_decode_tokens_kernel",
+            "fp32_peak_tflop_s": fp32_peak_tflops(mhz),
+            "fp32_peak_kind": "152 SMs x 128 FP32 lanes x 2 x SM clock (%s MHz)"
+                              % ("sampled %.0f" % mhz if mhz else "max 2070"),
+            "per_T": rows}
     if world == 1 and not args.no_cpu_baseline:
         gbs, n, el = oracle_decode_sample(stack.host0, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -665,6 +738,11 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the chunked-prefill measurement")
     ap.add_argument("--prefill-kernel", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor core")
+    ap.add_argument("--no-tokens", action="store_true",
+                    help="skip the multi-token decode leg")
+    ap.add_argument("--tokens-only", action="store_true",
+                    help="time only kda_decode_tokens at --M streams and --tokens-T tokens")
+    ap.add_argument("--tokens-T", type=int, default=4)
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill (with --prefill-M/--prefill-T), one JSON line")
     ap.add_argument("--prefill-M", type=int, default=4)
@@ -686,6 +764,15 @@ def main():
         return
     if args.sweep:
         sweep(args)
+        return
+    if args.tokens_only:
+        import torch
+        from linear_attention_decode_step_gb300 import build, inputs, kda
+        build.build()
+        ms = time_tokens(torch, kda, inputs, args.M, args.tokens_T, args.state_dtype, args.steps,
+                         args.warmup)
+        print(json.dumps(tokens_summary(ms, args.M, args.tokens_T, args.state_dtype,
+                                        measured_peak()[0], None)))
         return
     if args.prefill_only:
         import torch

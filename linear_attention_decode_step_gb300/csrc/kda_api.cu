@@ -271,12 +271,14 @@ kda_status kda_decode_tokens(const void *x, int x_dtype, const float *conv_w, vo
 kda_status kda_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);
-    unsigned int code = 0, code2 = 0;
+    unsigned int code = 0, code2 = 0, code3 = 0;
     e = kda::take_stream_error(&code);
     if (e != cudaSuccess) return cuda_status(e);
     e = kda::take_prefill_error(&code2);
     if (e != cudaSuccess) return cuda_status(e);
-    return (code | code2) ? KDA_ERR_TIMEOUT : KDA_OK;
+    e = kda::take_tokens_error(&code3);
+    if (e != cudaSuccess) return cuda_status(e);
+    return (code | code2 | code3) ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
 }  // extern "C"

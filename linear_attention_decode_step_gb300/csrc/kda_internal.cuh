@@ -84,6 +84,9 @@ void default_decode_config(int M, int H, int state_dtype, int *kernel, int *colu
 // Reads and clears the streaming kernel's device error word.
 cudaError_t take_stream_error(unsigned int *code);
 
+// Reads and clears the multi-token decode kernel's device error word.
+cudaError_t take_tokens_error(unsigned int *code);
+
 // Standalone short conv + SiLU for one token.
 cudaError_t launch_conv(const void *x, int x_dtype, const float *conv_w, void *cache,
                         float *y, int M, int D, cudaStream_t stream);
