@@ -11,16 +11,16 @@
 //   O  = scale ((e^G Q) S + P Delta)
 //   S  = Diag(e^{G_63}) S + (e^{G_63 - G} K)^T Delta
 //
-// Organisation. One CTA (256 threads) owns one (stream, head) and walks its
-// chunks in order. The state lives in tensor memory for the whole sequence,
-// transposed (lane = value channel j, column = key channel i) and in FP32:
-// it is the accumulator of the state update and, read as TF32, the A operand
-// (from tensor memory) of the products with S. Every MMA has M = 128 rows:
-//   MMA1  D1 = [L0; Lq0; L1; Lq1] [R0 | R1]^T     A and P, diagonal halves
-//   MMA2  D2 = [Lo; Lqo] R0^T                      A and P, rows 32-63 x cols 0-31
-//   MMA3  D3 = S^T [Kd; Qd]^T                       Y^T = (Kd S)^T and (Qd S)^T
-//   MMA4  D4 = Z^T M^T,  Z = V - Y                  Delta^T
-//   MMA5  D3[:, 64:] += Delta^T P^T                 O^T
+// Organisation. One CTA (512 threads, 16 warps) owns one (stream, head) and
+// walks its chunks in order. The state lives in tensor memory for the whole
+// sequence, transposed (lane = value channel j, column = key channel i) and
+// in FP32: it is the accumulator of the state update and, read as TF32, the
+// A operand (from tensor memory) of the products with S. Every MMA has
+// M = 128 rows:
+//   MMA1  D1 = [L0; Lq0; L1; Lq1] [R0; R1; R0o]^T     A and P (N = 96)
+//   MMA3  D3 = S^T [Kd; Qd]^T                           Y^T = (Kd S)^T and (Qd S)^T
+//   MMA4  D4 = Z^T M^T,  Z = V - Y                      Delta^T
+//   MMA5  D3[:, 64:] += Delta^T P^T                     O^T
 //   MMA6  S^T += Delta^T Kdec,  after S^T *= e^{G_63} per column
 // Operand tiles are written by the threads in the K-major core-matrix layout
 // (kda_umma.cuh) and read through shared-memory descriptors.
@@ -29,17 +29,27 @@
 // 32-token half (m_b = G_15, G_47): inside a half |G_r - m_b| spans at most 16
 // per-token log-decays, which stays inside FP32 for log(alpha) above about
 // -5.4 (the model's gate keeps it above -5; section 8.2.3 ties the -5 floor to
-// 16-token spans). Rows of the second half against columns of the first use
-// e^{G_r - m_0} <= 1 on the left and the first half's own right factor.
+// 16-token spans). The block of second-half rows against first-half columns
+// uses the second half's left factor and R0o = K e^{m_1 - G} <= 1 on the right.
 // Every factor of Kd, Qd, Kdec and the state decay is <= 1.
+//
+// Thread roles. "Token-channel" work (decay scan, norms, operand tiles): warp
+// w covers channels 16 (w % 8) .. + 15 and the 32-token half w / 8; lane
+// (qq, rr) = (lane / 8, lane % 8) holds tokens 8 g + rr (g = 0..3) of the half
+// and channels 4 qq .. + 3 of the warp's group. A quarter-warp (8 lanes, the
+// unit in which 16-byte shared-memory stores are served) thus writes the 8
+// rows of one core matrix: the tile stores are free of bank conflicts. "Tensor-memory" work: warp w
+// reads lanes 32 (w % 4) .. + 31 (value channel j) and column quarter w / 4.
 //
 // The unit lower-triangular inverse is taken on CUDA cores in 16 x 16 blocks:
 // diagonal blocks by forward substitution (one lane per column), off-diagonal
 // blocks level by level from the block recurrence T_RI = -T_RR sum_Q A_RQ T_QI.
 //
-// Inputs of the next chunk are loaded into registers while the current one is
-// processed. Every mbarrier wait is bounded; on timeout the kernel sets the
-// device error word (kda_device_error) and stops.
+// Inputs are loaded into registers ahead of use: q, k, alpha of the next
+// chunk once this chunk's operand tiles are built, v of this chunk while the
+// inverse is formed. O leaves through shared memory with bulk copies. Every mbarrier
+// wait is bounded; on timeout the kernel sets the device error word
+// (kda_device_error) and stops.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -59,7 +69,7 @@ namespace {
 
 constexpr int DK = kHeadDim;
 constexpr int C = 64;
-constexpr int NT = 256;
+constexpr int NT = 512;
 constexpr float kL2Eps = 1e-6f;
 constexpr long long kWaitBudget = 4000000000LL;
 
@@ -67,11 +77,10 @@ constexpr long long kWaitBudget = 4000000000LL;
 constexpr uint32_t KB128 = DK * 4;  // one row of a K = 128 tile
 constexpr uint32_t KB64 = C * 4;    // one row of a K = 64 tile
 // phase-1 tiles
-constexpr uint32_t T_LO = 0;                       // [Lo; Lqo]      64 x 128 (+64 rows overlap LA)
-constexpr uint32_t T_LA = T_LO + 64 * KB128;       // [L0;Lq0;L1;Lq1] 128 x 128
-constexpr uint32_t T_RB = T_LA + 128 * KB128;      // [R0; R1]        64 x 128
-constexpr uint32_t PH1_END = T_RB + 64 * KB128;    // 131072
-// phase-2 tiles (overlay phase-1 after MMA1/2 complete)
+constexpr uint32_t T_LA = 0;                       // [L0; Lq0; L1; Lq1]  128 x 128
+constexpr uint32_t T_RB = T_LA + 128 * KB128;      // [R0; R1; R0o]        96 x 128
+constexpr uint32_t PH1_END = T_RB + 96 * KB128;    // 114688
+// phase-2 tiles (overlay phase-1 once MMA1 has completed)
 constexpr uint32_t T_KQ = 0;                       // [Kd; Qd]       128 x 128
 constexpr uint32_t T_KDEC = T_KQ + 128 * KB128;    // Kdec^T          128 x 64
 constexpr uint32_t T_M = T_KDEC + 128 * KB64;      // M               64 x 64
@@ -80,20 +89,32 @@ constexpr uint32_t T_A = T_P + 64 * KB64;          // A (plain [64][68] FP32)
 constexpr int LDA = 68;
 constexpr uint32_t T_T = T_A + 64 * LDA * 4;       // T = (I + A)^-1 (plain [64][68] FP32)
 constexpr uint32_t T_X = T_T + 64 * LDA * 4;       // scratch: up to 3 blocks of 16 x 16
-constexpr int LDK = 144;                           // Kdec staging row: 128 + 16 (bank shift)
+constexpr int LDK = 132;                           // Kdec staging row: 128 + 4
 constexpr uint32_t T_KST = T_X + 3 * 256 * 4;      // Kdec, token-major staging [64][LDK]
 constexpr uint32_t PH2_END = T_KST + 64 * LDK * 4;
+constexpr uint32_t T_O = 0;                        // O staging [64][128] (phase 7, KQ is dead)
+static_assert(T_A >= PH1_END, "A and P are written while nothing reads phase-1 tiles");
 constexpr uint32_t TILES = PH2_END > PH1_END ? PH2_END : PH1_END;
 // small buffers (bytes)
-constexpr uint32_t S_NORM = TILES;                 // [2][8][64] partial sums of q^2, k^2
-constexpr uint32_t S_BETA = S_NORM + 2 * 8 * 64 * 4;
+constexpr int LDN = 12;                            // norm partials row: 8 groups + 4 (bank shift)
+constexpr uint32_t S_NORM = TILES;                 // [2][64 rows][LDN] partial sums of q^2, k^2
+constexpr uint32_t S_XCH = S_NORM + 2 * 64 * LDN * 4;  // [3][128]: G_31, L_47, L_63 per channel
+constexpr uint32_t S_BETA = S_XCH + 3 * 128 * 4;
 constexpr uint32_t S_GAM = S_BETA + 64 * 4;        // [128] e^{G_63}
 constexpr uint32_t S_BAR = S_GAM + 128 * 4;        // 4 mbarriers
 constexpr uint32_t S_SLOT = S_BAR + 4 * 8;
 constexpr uint32_t SMEM_BYTES = S_SLOT + 16;
+static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in shared memory");
+
+// the thread that issues every MMA: lane 0 of the last warp (free of the
+// phase-specific work that warps 0-1 carry in the inverse)
+constexpr int kIssuer = NT - 32;
+// named barriers (0 is __syncthreads): the issuer waits for all threads,
+// the others only signal and move on
+constexpr uint32_t kBarMma1 = 1, kBarMma3 = 2, kBarOut = 3;
 
 // TMEM columns
-constexpr uint32_t TM_S = 0, TM_D3 = 128, TM_Z = 256, TM_D4 = 320, TM_D1 = 384, TM_D2 = 448;
+constexpr uint32_t TM_S = 0, TM_D3 = 128, TM_Z = 256, TM_D4 = 320, TM_D1 = 384;
 constexpr uint32_t TM_COLS = 512;
 
 __device__ __forceinline__ void raise_error(unsigned int code) { atomicOr(&g_prefill_error, code); }
@@ -109,24 +130,6 @@ __device__ __forceinline__ float lg2(float x) {
     return y;
 }
 
-// 4 consecutive input elements -> floats
-__device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&f)[4]) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
-    f[0] = __uint_as_float(u.x << 16);
-    f[1] = __uint_as_float(u.x & 0xffff0000u);
-    f[2] = __uint_as_float(u.y << 16);
-    f[3] = __uint_as_float(u.y & 0xffff0000u);
-}
-__device__ __forceinline__ void load4(const float *p, float (&f)[4]) {
-    const float4 u = __ldg(reinterpret_cast<const float4 *>(p));
-    f[0] = u.x;
-    f[1] = u.y;
-    f[2] = u.z;
-    f[3] = u.w;
-}
-__device__ __forceinline__ float load1(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
-__device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
-
 // FP32 -> TF32, round to nearest (ties away from zero), by adding half a
 // TF32 ulp to the magnitude bits and clearing the 13 bits TF32 drops. The
 // tensor cores read an FP32 operand as TF32 by ignoring those bits, a biased
@@ -141,14 +144,10 @@ __device__ __forceinline__ void st_tile4(unsigned char *tile, uint32_t row, uint
     *reinterpret_cast<float4 *>(tile + (row >> 3) * (8u * kbytes) + c4 * 128u + (row & 7u) * 16u) =
         make_float4(tf32r(a), tf32r(b), tf32r(c), tf32r(d));
 }
-__device__ __forceinline__ void st_tile1(unsigned char *tile, uint32_t row, uint32_t k,
-                                         uint32_t kbytes, float v) {
-    *reinterpret_cast<float *>(tile + umma::kmajor_offset(row, k, 4, kbytes)) = tf32r(v);
-}
 
 // Per-thread inputs of one chunk, kept exactly as loaded (no arithmetic on
 // them until the chunk is processed, so the loads overlap the previous
-// chunk's work): rows r = 8 rg + rr, channels 4 c4 + e.
+// chunk's work).
 template <typename TQ> struct Raw;
 template <> struct Raw<__nv_bfloat16> {
     typedef uint2 Q4;              // 4 BF16
@@ -185,44 +184,43 @@ template <> struct Raw<float> {
     __device__ __forceinline__ static V1 zero1() { return 0.f; }
 };
 
+// q, k, alpha of this thread's 4 tokens x 4 channels (token-channel mapping);
+// tokens past T read as q = k = 0, alpha = 1
 template <typename TQ>
-struct ChunkRegs {
-    typename Raw<TQ>::Q4 q[8], k[8];
-    float4 al[8];                      // alpha (linear); 1 on padding rows
-    typename Raw<TQ>::V1 v[32];        // v[r][j], r = 32 hw + i, j = 32 q4 + lane
-    float beta;                        // beta of token tid (tid < 64)
+struct QKA {
+    typename Raw<TQ>::Q4 q[4], k[4];
+    float4 al[4];
 };
-
 template <typename TQ>
-__device__ __forceinline__ void load_chunk(ChunkRegs<TQ> &R, const PrefillArgs &a, int m, int h,
-                                           int c0, int rr, int c4, int q4, int hw, int lane, int tid) {
+__device__ __forceinline__ void load_qka(QKA<TQ> &R, const PrefillArgs &a, int m, int h, int t0,
+                                         int c4) {
     using RW = Raw<TQ>;
     const TQ *q = static_cast<const TQ *>(a.q);
     const TQ *k = static_cast<const TQ *>(a.k);
-    const TQ *v = static_cast<const TQ *>(a.v);
-    const int T = a.T, H = a.H;
 #pragma unroll
-    for (int rg = 0; rg < 8; ++rg) {
-        const int t = c0 + 8 * rg + rr;
-        if (t < T) {
-            const size_t base = (((size_t)m * T + t) * H + h) * DK + 4 * c4;
-            R.q[rg] = RW::load4(q + base);
-            R.k[rg] = RW::load4(k + base);
-            R.al[rg] = __ldg(reinterpret_cast<const float4 *>(a.alpha + base));
+    for (int g = 0; g < 4; ++g) {
+        const int t = t0 + 8 * g;
+        if (t < a.T) {
+            const size_t base = (((size_t)m * a.T + t) * a.H + h) * DK + 4 * c4;
+            R.q[g] = RW::load4(q + base);
+            R.k[g] = RW::load4(k + base);
+            R.al[g] = __ldg(reinterpret_cast<const float4 *>(a.alpha + base));
         } else {
-            R.q[rg] = R.k[rg] = typename RW::Q4{};
-            R.al[rg] = make_float4(1.f, 1.f, 1.f, 1.f);
+            R.q[g] = R.k[g] = typename RW::Q4{};
+            R.al[g] = make_float4(1.f, 1.f, 1.f, 1.f);
         }
     }
+}
+// v of 16 tokens t0 .. t0 + 15 at value channel j (tensor-memory mapping)
+template <typename TQ>
+__device__ __forceinline__ void load_v(typename Raw<TQ>::V1 (&v)[16], const PrefillArgs &a, int m,
+                                       int h, int t0, int j) {
+    using RW = Raw<TQ>;
+    const TQ *vp = static_cast<const TQ *>(a.v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int t = c0 + 32 * hw + i;
-        R.v[i] = t < T ? RW::load1(v + (((size_t)m * T + t) * H + h) * DK + 32 * q4 + lane)
-                       : RW::zero1();
-    }
-    if (tid < C) {
-        const int t = c0 + tid;
-        R.beta = t < T ? __ldg(a.beta + ((size_t)m * T + t) * H + h) : 0.f;
+    for (int i = 0; i < 16; ++i) {
+        const int t = t0 + i;
+        v[i] = t < a.T ? RW::load1(vp + (((size_t)m * a.T + t) * a.H + h) * DK + j) : RW::zero1();
     }
 }
 
@@ -230,20 +228,26 @@ template <typename TQ>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     float *sNorm = reinterpret_cast<float *>(sm + S_NORM);
+    float *sXch = reinterpret_cast<float *>(sm + S_XCH);
     float *sBeta = reinterpret_cast<float *>(sm + S_BETA);
     float *sGam = reinterpret_cast<float *>(sm + S_GAM);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);  // 0: MMA1/2, 1: MMA3, 2: MMA4, 3: MMA5/6
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);  // 0: MMA1, 1: MMA3, 2: MMA4, 3: MMA5/6
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + S_SLOT);
     float *sA = reinterpret_cast<float *>(sm + T_A);
     float *sT = reinterpret_cast<float *>(sm + T_T);
     float *sX = reinterpret_cast<float *>(sm + T_X);
     float *sKst = reinterpret_cast<float *>(sm + T_KST);
+    float *sO = reinterpret_cast<float *>(sm + T_O);
 
     const int h = blockIdx.x % a.H, m = blockIdx.x / a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rr = lane >> 2, qq = lane & 3, c4 = 4 * warp + qq;  // token-channel mapping
-    const int q4 = warp & 3, hw = warp >> 2;                        // TMEM lane quarter, half
-    const int j = 32 * q4 + lane;                                   // value channel (TMEM lane)
+    // token-channel mapping
+    const int cg = warp & 7, rh = warp >> 3, rr = lane & 7, qq = lane >> 3;
+    const int c4 = 4 * cg + qq;                    // channels 4 c4 .. 4 c4 + 3
+    const int r0 = 32 * rh + rr;                   // tokens r0 + 8 g, g = 0..3
+    // tensor-memory mapping
+    const int q4 = warp & 3, hq = warp >> 2;
+    const int j = 32 * q4 + lane;                  // value channel (TMEM lane)
     const int T = a.T;
     const uint32_t sbase = ptx::smem_u32(sm);
 
@@ -261,9 +265,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const uint32_t tb = *slot;
     const uint32_t tq = tb + ((uint32_t)(32 * q4) << 16);  // this warp's TMEM lane quarter
 
-    // state in: S^T[j][i] = S[i][j]; this thread: lane j, key channels [64 hw, 64 hw + 64)
+    // state in: S^T[j][i] = S[i][j]; this thread: lane j, key channels [32 hq, 32 hq + 32)
     float *state = a.state + ((size_t)m * a.H + h) * DK * DK;
-    for (int c = 64 * hw; c < 64 * hw + 64; c += 8) {
+    for (int c = 32 * hq; c < 32 * hq + 32; c += 8) {
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) v8[e] = state[(size_t)(c + e) * DK + j];
@@ -272,134 +276,154 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     umma::wait_st();
 
     using RW = Raw<TQ>;
-    ChunkRegs<TQ> R;
-    load_chunk<TQ>(R, a, m, h, 0, rr, c4, q4, hw, lane, tid);
+    QKA<TQ> R;
+    float beta_n = 0.f;
+    load_qka<TQ>(R, a, m, h, r0, c4);
+    if (tid < C) beta_n = tid < T ? __ldg(a.beta + ((size_t)m * T + tid) * a.H + h) : 0.f;
 
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
+    const uint32_t id96 = umma::instr_desc(128, 96, umma::kFmtTF32);
     const uint32_t id64 = umma::instr_desc(128, 64, umma::kFmtTF32);
-    const uint32_t id32 = umma::instr_desc(128, 32, umma::kFmtTF32);
     bool ok = true;
     int phase = 0;
 
     for (int c0 = 0; c0 < T && ok; c0 += C, phase ^= 1) {
         // ---------------------------------------------------------- 1. decay, norms
-        // cumulative log2-decay over the chunk's rows (rows across lanes rr, then rg)
-        float G[8][4], qf[8][4], kf[8][4];
+        // cumulative log2-decay over the half's 32 tokens (lanes rr, then g)
+        float G[4][4], qf[4][4], kf[4][4];
 #pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
-            RW::widen4(R.q[rg], qf[rg]);
-            RW::widen4(R.k[rg], kf[rg]);
-            G[rg][0] = lg2(R.al[rg].x);
-            G[rg][1] = lg2(R.al[rg].y);
-            G[rg][2] = lg2(R.al[rg].z);
-            G[rg][3] = lg2(R.al[rg].w);
+        for (int g = 0; g < 4; ++g) {
+            RW::widen4(R.q[g], qf[g]);
+            RW::widen4(R.k[g], kf[g]);
+            G[g][0] = lg2(R.al[g].x);
+            G[g][1] = lg2(R.al[g].y);
+            G[g][2] = lg2(R.al[g].z);
+            G[g][3] = lg2(R.al[g].w);
         }
         float carry[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
+        for (int g = 0; g < 4; ++g) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float x = G[rg][e];
+                float x = G[g][e];
 #pragma unroll
-                for (int d = 4; d < 32; d <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, d);
-                    if (lane >= d) x += y;
+                for (int d = 1; d < 8; d <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, d, 8);
+                    if (rr >= d) x += y;
                 }
                 x += carry[e];
-                G[rg][e] = x;
-                carry[e] = __shfl_sync(0xffffffffu, x, 28 + qq);
+                G[g][e] = x;
+                carry[e] = __shfl_sync(0xffffffffu, x, 8 * qq + 7);
             }
         }
-        // references: m0 = G_15, m1 = G_47, e63 = G_63 (log2 units), from lanes rr = 7
-        float m0[4], m1[4], e63[4];
+        // mid (token 15 of the half) and total (token 31), from lanes rr = 7
+        float mid[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            m0[e] = __shfl_sync(0xffffffffu, G[1][e], 28 + qq);
-            m1[e] = __shfl_sync(0xffffffffu, G[5][e], 28 + qq);
-            e63[e] = carry[e];
+        for (int e = 0; e < 4; ++e) mid[e] = __shfl_sync(0xffffffffu, G[1][e], 8 * qq + 7);
+        if (rr == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (rh == 0) {
+                    sXch[4 * c4 + e] = carry[e];              // G_31
+                } else {
+                    sXch[128 + 4 * c4 + e] = mid[e];          // L_47 = G_47 - G_31
+                    sXch[256 + 4 * c4 + e] = carry[e];        // L_63 = G_63 - G_31
+                }
+            }
         }
         // L2-norm partial sums: 4 channels here, 16 per warp
 #pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
+        for (int g = 0; g < 4; ++g) {
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                sq = fmaf(qf[rg][e], qf[rg][e], sq);
-                sk = fmaf(kf[rg][e], kf[rg][e], sk);
+                sq = fmaf(qf[g][e], qf[g][e], sq);
+                sk = fmaf(kf[g][e], kf[g][e], sk);
             }
-            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-            sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-            sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 16);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 8);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 16);
             if (qq == 0) {
-                sNorm[(0 * 8 + warp) * 64 + 8 * rg + rr] = sq;
-                sNorm[(1 * 8 + warp) * 64 + 8 * rg + rr] = sk;
+                const int r = r0 + 8 * g;
+                sNorm[(0 * 64 + r) * LDN + cg] = sq;
+                sNorm[(1 * 64 + r) * LDN + cg] = sk;
             }
         }
-        if (tid < C) sBeta[tid] = R.beta;
-        if (rr == 0 && warp < 8) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sGam[4 * c4 + e] = ex2(e63[e]);
-        }
+        if (tid < C) sBeta[tid] = beta_n;
+        // the previous chunk's O staging (at the start of the operand tiles) has been read
+        if (warp == 0 && c0 > 0) ptx::bulk_wait_read_all();
         __syncthreads();
-        float rq[8], rk[8];
+        float rq[4], rk[4];
 #pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
-            float sq = 0.f, sk = 0.f;
+        for (int g = 0; g < 4; ++g) {
+            const int r = r0 + 8 * g;
+            const float4 qa = *reinterpret_cast<const float4 *>(sNorm + r * LDN);
+            const float4 qb = *reinterpret_cast<const float4 *>(sNorm + r * LDN + 4);
+            const float4 ka = *reinterpret_cast<const float4 *>(sNorm + (64 + r) * LDN);
+            const float4 kb = *reinterpret_cast<const float4 *>(sNorm + (64 + r) * LDN + 4);
+            rq[g] = 1.0f / sqrtf(qa.x + qa.y + qa.z + qa.w + qb.x + qb.y + qb.z + qb.w + kL2Eps);
+            rk[g] = 1.0f / sqrtf(ka.x + ka.y + ka.z + ka.w + kb.x + kb.y + kb.z + kb.w + kL2Eps);
+        }
+        // per-channel factors (log2 units):
+        //   half 0: u = e^{G - G_15};  R0o = R e^{G_31 + L_47 - G_15};
+        //           Kd = L e^{G_15};   Kdec = R e^{G_31 + L_63 - G_15}
+        //   half 1: u = e^{L - L_47};  Kd = L e^{G_31 + L_47};  Kdec = R e^{L_63 - L_47}
+        float fo[4], em[4], ed[4];
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                sq += sNorm[(0 * 8 + w) * 64 + 8 * rg + rr];
-                sk += sNorm[(1 * 8 + w) * 64 + 8 * rg + rr];
+        for (int e = 0; e < 4; ++e) {
+            const float g31 = sXch[4 * c4 + e], l47 = sXch[128 + 4 * c4 + e];
+            const float l63 = sXch[256 + 4 * c4 + e];
+            if (rh == 0) {
+                fo[e] = ex2(g31 + l47 - mid[e]);
+                em[e] = ex2(mid[e]);
+                ed[e] = ex2(g31 + l63 - mid[e]);
+            } else {
+                fo[e] = 0.f;
+                em[e] = ex2(g31 + l47);
+                ed[e] = ex2(l63 - l47);
             }
-            rq[rg] = 1.0f / sqrtf(sq + kL2Eps);
-            rk[rg] = 1.0f / sqrtf(sk + kL2Eps);
+        }
+        if (rh == 0 && rr == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sGam[4 * c4 + e] = ex2(sXch[4 * c4 + e] + sXch[256 + 4 * c4 + e]);
         }
 
         // ---------------------------------------------------------- 2. A / P operands
-        // u = e^{G - m_b} (>= 1 in the first quarter of a half, <= 1 after),
-        // L = K u, Lq = Q u, R = K / u; rows of the second half also get
-        // Lo = L e^{m1 - m0}, Lqo = Lq e^{m1 - m0} (= K e^{G - m0} <= 1).
-        float f10[4];
+        // L = K u, Lq = Q u, R = K / u (normalised q, k); kept for the state-pass operands
+        float Lk[4][4], Lq[4][4], Rk[4][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) f10[e] = ex2(m1[e] - m0[e]);
-#pragma unroll
-        for (int rg = 0; rg < 8; ++rg) {
-            const int r = 8 * rg + rr;
-            const bool second = rg >= 4;
-            float L[4], Lq[4], Rr[4];
+        for (int g = 0; g < 4; ++g) {
+            const int r = r0 + 8 * g;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float x = G[rg][e] - (second ? m1[e] : m0[e]);
+                const float x = G[g][e] - mid[e];
                 const float u = ex2(x), ui = ex2(-x);
-                const float kh = kf[rg][e] * rk[rg], qh = qf[rg][e] * rq[rg];
-                L[e] = kh * u;
-                Lq[e] = qh * u;
-                Rr[e] = kh * ui;
+                const float kh = kf[g][e] * rk[g];
+                Lk[g][e] = kh * u;
+                Lq[g][e] = qf[g][e] * rq[g] * u;
+                Rk[g][e] = kh * ui;
             }
-            const int rowL = second ? r + 32 : r, rowLq = second ? r + 64 : r + 32;
-            st_tile4(sm + T_LA, rowL, c4, KB128, L[0], L[1], L[2], L[3]);
-            st_tile4(sm + T_LA, rowLq, c4, KB128, Lq[0], Lq[1], Lq[2], Lq[3]);
-            st_tile4(sm + T_RB, r, c4, KB128, Rr[0], Rr[1], Rr[2], Rr[3]);
-            if (second) {
-                st_tile4(sm + T_LO, r - 32, c4, KB128, L[0] * f10[0], L[1] * f10[1], L[2] * f10[2],
-                         L[3] * f10[3]);
-                st_tile4(sm + T_LO, r, c4, KB128, Lq[0] * f10[0], Lq[1] * f10[1], Lq[2] * f10[2],
-                         Lq[3] * f10[3]);
-            }
+            const int rowL = rh ? r + 32 : r, rowLq = rh ? r + 64 : r + 32;
+            st_tile4(sm + T_LA, rowL, c4, KB128, Lk[g][0], Lk[g][1], Lk[g][2], Lk[g][3]);
+            st_tile4(sm + T_LA, rowLq, c4, KB128, Lq[g][0], Lq[g][1], Lq[g][2], Lq[g][3]);
+            st_tile4(sm + T_RB, r, c4, KB128, Rk[g][0], Rk[g][1], Rk[g][2], Rk[g][3]);
+            if (rh == 0)
+                st_tile4(sm + T_RB, 64 + r, c4, KB128, Rk[g][0] * fo[0], Rk[g][1] * fo[1],
+                         Rk[g][2] * fo[2], Rk[g][3] * fo[3]);
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
-        if (tid == 0) {
+        if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma1, NT);
+        else ptx::named_bar_arrive(kBarMma1, NT);
+        if (tid == kIssuer) {
+            umma::fence_after_sync();
 #pragma unroll 1
-            for (int ks = 0; ks < DK / 8; ++ks) {
-                const uint64_t bd = umma::smem_desc(sbase + T_RB + ks * 256, 128, 8 * KB128);
-                umma::mma_ss(tb + TM_D1, umma::smem_desc(sbase + T_LA + ks * 256, 128, 8 * KB128), bd,
-                             id64, ks > 0, 1);
-                umma::mma_ss(tb + TM_D2, umma::smem_desc(sbase + T_LO + ks * 256, 128, 8 * KB128), bd,
-                             id32, ks > 0, 1);
-            }
+            for (int ks = 0; ks < DK / 8; ++ks)
+                umma::mma_ss(tb + TM_D1, umma::smem_desc(sbase + T_LA + ks * 256, 128, 8 * KB128),
+                             umma::smem_desc(sbase + T_RB + ks * 256, 128, 8 * KB128), id96, ks > 0,
+                             1);
             umma::commit(&bar[0]);
         }
         if (!ptx::mbar_wait(&bar[0], phase, kWaitBudget)) {
@@ -410,98 +434,78 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_after_sync();
 
         // ---------------------------------------------------------- 3. A, P from TMEM
-        // warp (q4, hw): q4 = 0 A-rows, 1 P-rows of the first half (D1) or, with
-        // hw = 1, of rows 32-63 x columns 0-31 (D2); q4 = 2, 3: second half (D1).
+        // lane quarter q4: 0 A rows 0-31, 1 P rows 0-31, 2 A rows 32-63, 3 P rows 32-63.
+        // D1 columns: 0-31 first-half columns (relative to m_0), 32-63 second-half
+        // columns, 64-95 first-half columns relative to m_1 (for second-half rows).
         {
             const bool isP = q4 & 1;
-            int r, i0;
-            uint32_t col;
-            bool active = true;
-            if (hw == 0) {
-                r = (q4 < 2 ? 0 : 32) + lane;
-                i0 = q4 < 2 ? 0 : 32;
-                col = TM_D1 + i0;
-            } else {
-                r = 32 + lane;
-                i0 = 0;
-                col = TM_D2;
-                active = q4 < 2;
-            }
-            if (active) {
-                const float br = sBeta[r];
-                float d[32];
-                umma::ld_x32(tq + col, d);
-                umma::wait_ld();
+            const int r = (q4 < 2 ? 0 : 32) + lane;
+            const float br = sBeta[r];
+            auto put4 = [&](int s, const float *d) {  // columns s .. s + 3 of row r
+                float v4[4];
 #pragma unroll
-                for (int cb = 0; cb < 32; cb += 4) {
-                    float v4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = i0 + cb + e;
-                        v4[e] = isP ? (i <= r ? d[cb + e] : 0.f) : (i < r ? br * d[cb + e] : 0.f);
-                    }
-                    if (isP)
-                        st_tile4(sm + T_P, r, (i0 + cb) >> 2, KB64, v4[0], v4[1], v4[2], v4[3]);
-                    else
-                        *reinterpret_cast<float4 *>(sA + r * LDA + i0 + cb) =
-                            make_float4(v4[0], v4[1], v4[2], v4[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const int i = s + e;
+                    v4[e] = isP ? (i <= r ? d[e] : 0.f) : (i < r ? br * d[e] : 0.f);
                 }
-            } else if (q4 == 3) {  // P rows 0-31, columns 32-63 are zero
+                if (isP)
+                    st_tile4(sm + T_P, r, s >> 2, KB64, v4[0], v4[1], v4[2], v4[3]);
+                else
+                    *reinterpret_cast<float4 *>(sA + r * LDA + s) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+            };
+            if (q4 < 2) {
+                float d[8];
+                umma::ld_x8(tq + TM_D1 + 8 * hq, d);
+                umma::wait_ld();
+                put4(8 * hq, d);
+                put4(8 * hq + 4, d + 4);
+                if (isP) {  // P rows 0-31, columns 32-63 are zero
+                    st_tile4(sm + T_P, r, (32 + 8 * hq) >> 2, KB64, 0.f, 0.f, 0.f, 0.f);
+                    st_tile4(sm + T_P, r, (36 + 8 * hq) >> 2, KB64, 0.f, 0.f, 0.f, 0.f);
+                }
+            } else {
+                float d[16];
+                umma::ld_x16(tq + TM_D1 + 32 + 16 * hq, d);
+                umma::wait_ld();
+                const int s0 = hq < 2 ? 32 + 16 * hq : 16 * (hq - 2);
 #pragma unroll
-                for (int cb = 32; cb < 64; cb += 4) st_tile4(sm + T_P, lane, cb >> 2, KB64, 0.f, 0.f, 0.f, 0.f);
+                for (int b = 0; b < 4; ++b) put4(s0 + 4 * b, d + 4 * b);
             }
         }
         umma::fence_before_sync();
-        __syncthreads();  // A, P visible; MMA1/2 operands may now be overwritten
+        __syncthreads();  // A, P visible; MMA1 operands may now be overwritten
 
         // ---------------------------------------------------------- 4. state-pass operands
-        //   Kd = K e^G = (K u) e^{m_b},   Qd = Q e^G,   Kdec = K e^{G63 - G} = (K / u) e^{G63 - m_b}
-        {
-            float em0[4], em1[4], ed0[4], ed1[4];
+        //   Kd = K e^G = L em,   Qd = Lq em,   Kdec = K e^{G63 - G} = R ed
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                em0[e] = ex2(m0[e]);
-                em1[e] = ex2(m1[e]);
-                ed0[e] = ex2(e63[e] - m0[e]);
-                ed1[e] = ex2(e63[e] - m1[e]);
-            }
-#pragma unroll
-            for (int rg = 0; rg < 8; ++rg) {
-                const int r = 8 * rg + rr;
-                const bool second = rg >= 4;
-                float Kd[4], Qd[4], Kc[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x = G[rg][e] - (second ? m1[e] : m0[e]);
-                    const float u = ex2(x), ui = ex2(-x);
-                    const float kh = kf[rg][e] * rk[rg], qh = qf[rg][e] * rq[rg];
-                    const float em = second ? em1[e] : em0[e];
-                    Kd[e] = kh * u * em;
-                    Qd[e] = qh * u * em;
-                    Kc[e] = kh * ui * (second ? ed1[e] : ed0[e]);
-                }
-                st_tile4(sm + T_KQ, r, c4, KB128, Kd[0], Kd[1], Kd[2], Kd[3]);
-                st_tile4(sm + T_KQ, 64 + r, c4, KB128, Qd[0], Qd[1], Qd[2], Qd[3]);
-                *reinterpret_cast<float4 *>(sKst + r * LDK + 4 * c4) =
-                    make_float4(Kc[0], Kc[1], Kc[2], Kc[3]);
-            }
+        for (int g = 0; g < 4; ++g) {
+            const int r = r0 + 8 * g;
+            st_tile4(sm + T_KQ, r, c4, KB128, Lk[g][0] * em[0], Lk[g][1] * em[1], Lk[g][2] * em[2],
+                     Lk[g][3] * em[3]);
+            st_tile4(sm + T_KQ, 64 + r, c4, KB128, Lq[g][0] * em[0], Lq[g][1] * em[1],
+                     Lq[g][2] * em[2], Lq[g][3] * em[3]);
+            *reinterpret_cast<float4 *>(sKst + r * LDK + 4 * c4) =
+                make_float4(Rk[g][0] * ed[0], Rk[g][1] * ed[1], Rk[g][2] * ed[2], Rk[g][3] * ed[3]);
         }
         __syncthreads();
+        // the next chunk's q, k, alpha (the registers of this one are consumed)
+        if (c0 + C < T) load_qka<TQ>(R, a, m, h, c0 + C + r0, c4);
         // Kdec^T tile (row = key channel c, K = token): 16-byte row segments,
         // 8 consecutive channels per quarter-warp (one core matrix)
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
+        for (int it = 0; it < 4; ++it) {
             const int u = it * NT + tid;
-            const int c8 = u & 7, kq = (u >> 3) & 15, cg = u >> 7;
-            const int c = 8 * cg + c8;
+            const int c8 = u & 7, kq = (u >> 3) & 15, cgr = u >> 7;
+            const int c = 8 * cgr + c8;
             st_tile4(sm + T_KDEC, c, kq, KB64, sKst[(4 * kq + 0) * LDK + c], sKst[(4 * kq + 1) * LDK + c],
                      sKst[(4 * kq + 2) * LDK + c], sKst[(4 * kq + 3) * LDK + c]);
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
-        if (tid == 0) {
+        if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma3, NT);
+        else ptx::named_bar_arrive(kBarMma3, NT);
+        if (tid == kIssuer) {
+            umma::fence_after_sync();
 #pragma unroll 1
             for (int ks = 0; ks < DK / 8; ++ks)
                 umma::mma_ts(tb + TM_D3, tb + TM_S + ks * 8,
@@ -510,17 +514,23 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
 
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
-        // (runs on CUDA cores while MMA3 is on the tensor cores)
+        // (runs on CUDA cores while MMA3 is on the tensor cores; v of this
+        // chunk is loaded meanwhile)
+        typename RW::V1 vr[16];
+        load_v<TQ>(vr, a, m, h, c0 + 16 * hq, j);
         // 5a. diagonal 16 x 16 blocks, one lane per column: T_bb = (I + A_bb)^-1
         if (warp < 2) {
             const int b = 2 * warp + (lane >> 4), jj = lane & 15, j0 = 16 * b;
             float tcol[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                float x = r == jj ? 1.f : 0.f;
+                float x0 = r == jj ? 1.f : 0.f, x1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) x = fmaf(-sA[(j0 + r) * LDA + j0 + i], tcol[i], x);
-                tcol[r] = r >= jj ? x : 0.f;
+                for (int i = 0; i < r; i += 2) {
+                    x0 = fmaf(-sA[(j0 + r) * LDA + j0 + i], tcol[i], x0);
+                    if (i + 1 < r) x1 = fmaf(-sA[(j0 + r) * LDA + j0 + i + 1], tcol[i + 1], x1);
+                }
+                tcol[r] = r >= jj ? x0 + x1 : 0.f;
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) sT[(j0 + r) * LDA + j0 + jj] = tcol[r];
@@ -568,7 +578,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         // 5c. M[r][i] = T[r][i] beta_i (lower with diagonal) into the operand tile
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < 2; ++it) {
             const int u = it * NT + tid;
             const int r = 8 * (u >> 7) + (u & 7), iq = (u >> 3) & 15, i = 4 * iq;
             const float4 tv = *reinterpret_cast<const float4 *>(sT + r * LDA + i);
@@ -577,6 +587,11 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                      i + 2 <= r ? tv.z * bv.z : 0.f, i + 3 <= r ? tv.w * bv.w : 0.f);
         }
         umma::fence_smem_to_async();
+        // the next chunk's beta (sBeta of this chunk has been read)
+        if (tid < C) {
+            const int t = c0 + C + tid;
+            beta_n = t < T ? __ldg(a.beta + ((size_t)m * T + t) * a.H + h) : 0.f;
+        }
 
         // ---------------------------------------------------------- 6. Z = V - Y, decay S
         if (!ptx::mbar_wait(&bar[1], phase, kWaitBudget)) {
@@ -586,31 +601,27 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         umma::fence_after_sync();
         {
-            float y[32];  // rows r = 32 hw .. 32 hw + 31
-            umma::ld_x32(tq + TM_D3 + 32 * hw, y);
+            float y[16];  // tokens 16 hq .. 16 hq + 15
+            umma::ld_x16(tq + TM_D3 + 16 * hq, y);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) y[e] = tf32r(RW::widen1(R.v[e]) - y[e]);
-            umma::st_x32(tq + TM_Z + 32 * hw, y);
+            for (int e = 0; e < 16; ++e) y[e] = tf32r(RW::widen1(vr[e]) - y[e]);
+            umma::st_x16(tq + TM_Z + 16 * hq, y);
         }
-#pragma unroll
-        for (int c = 64 * hw; c < 64 * hw + 64; c += 32) {  // S^T[j][c] *= e^{G63_c}
+        {  // S^T[j][c] *= e^{G63_c}
             float s32[32];
-            umma::ld_x32(tq + TM_S + c, s32);
+            umma::ld_x32(tq + TM_S + 32 * hq, s32);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) s32[e] *= sGam[c + e];
-            umma::st_x32(tq + TM_S + c, s32);
+            for (int e = 0; e < 32; ++e) s32[e] *= sGam[32 * hq + e];
+            umma::st_x32(tq + TM_S + 32 * hq, s32);
         }
         umma::wait_st();
-
-        // prefetch the next chunk's inputs (registers are free now)
-        if (c0 + C < T) load_chunk<TQ>(R, a, m, h, c0 + C, rr, c4, q4, hw, lane, tid);
 
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
-        if (tid == 0) {
+        if (tid == kIssuer) {
 #pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks)
                 umma::mma_ts(tb + TM_D4, tb + TM_Z + ks * 8,
@@ -638,24 +649,33 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_after_sync();
 
         // ---------------------------------------------------------- 7. O out
+        // O^T (tokens 16 hq .. + 15 at value channel j) -> staging rows -> bulk copies
         {
-            float o32[32];
-            umma::ld_x32(tq + TM_D3 + 64 + 32 * hw, o32);
+            float o16[16];
+            umma::ld_x16(tq + TM_D3 + 64 + 16 * hq, o16);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int t = c0 + 32 * hw + e;
-                if (t < T) a.o[(((size_t)m * T + t) * a.H + h) * DK + j] = a.scale * o32[e];
-            }
+            for (int e = 0; e < 16; ++e) sO[(16 * hq + e) * DK + j] = a.scale * o16[e];
         }
+        umma::fence_smem_to_async();
         umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
+        if (warp == 0) ptx::named_bar_sync(kBarOut, NT);
+        else ptx::named_bar_arrive(kBarOut, NT);
+        if (warp == 0) {
+            const int nt = T - c0 < C ? T - c0 : C;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = lane + 32 * e;
+                if (t < nt)
+                    ptx::bulk_s2g(a.o + (((size_t)m * T + c0 + t) * a.H + h) * DK, sO + t * DK, DK * 4);
+            }
+            ptx::bulk_commit();
+        }
     }
 
     // state out
     if (ok) {
-        for (int c = 64 * hw; c < 64 * hw + 64; c += 8) {
+        for (int c = 32 * hq; c < 32 * hq + 32; c += 8) {
             float v8[8];
             umma::ld_x8(tq + TM_S + c, v8);
             umma::wait_ld();
@@ -663,6 +683,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             for (int e = 0; e < 8; ++e) state[(size_t)(c + e) * DK + j] = v8[e];
         }
     }
+    if (warp == 0) ptx::bulk_wait_all();  // O copies complete before the CTA's shared memory goes
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tb, TM_COLS);
