@@ -229,6 +229,40 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qk
                              float scale, int M, int T, int H, int dk, int dv, int chunk,
                              void *stream);
 
+/*
+ * kda_prefill_layer — a KDA layer over a prompt of T tokens for M streams, one
+ * launch on the tensor cores: the short conv + SiLU of the pre-conv q, k, v
+ * with the conv cache as left context, the forget gate from its raw input
+ * (in log space), L2 norm of q and k, the chunked recurrence ("GLM-5.3 deep
+ * dive" sections 8.2.3 - 8.2.5) and, optionally, the gated RMSNorm on every
+ * output (8.2.4 step 7). The result equals T calls of kda_decode_step_fused.
+ *
+ *   x           [M, T, 3, H*dk]  pre-conv q, k, v of the T tokens (x_dtype)
+ *   conv_w      [3, H*dk, 4]     FP32 conv weights (as kda_conv_step)
+ *   conv_cache  [M, 3, 3, H*dk]  in place; afterwards it holds the last three
+ *                                inputs of (cache, x_0 .. x_{T-1})
+ *   gate_f      [M, T, H, dk]    FP32 raw forget-gate input:
+ *                                log alpha = lb * sigmoid(exp(A_log[h]) * (f + dt_bias[h*dk + i]))
+ *   A_log [H], dt_bias [H * dk], gate_lower_bound (lb, -5 in GLM-5.3-Flash)
+ *   beta        [M, T, H]        FP32
+ *   state       [M, H, dk, dv]   FP32, in place
+ *   out_gate    [M, T, H, dv]    FP32 output-gate input, or NULL for no norm
+ *   norm_weight [dv], norm_eps   RMSNorm weight and eps (with out_gate)
+ *   y           [M, T, H, dv]    FP32 output (o, or its gated RMSNorm)
+ *   dk = dv = 128, chunk = 64 (KDA_ERR_UNSUPPORTED otherwise); cache_dtype ==
+ *   x_dtype. The tensor-core arithmetic is TF32 with FP32 accumulation, as in
+ *   kda_chunk_prefill, whose decay domain it shares (the gate keeps per-token
+ *   log alpha above lb).
+ * y, state and conv_cache must not overlap each other or any input.
+ */
+kda_status kda_prefill_layer(const void *x, int x_dtype, const float *conv_w,
+                             void *conv_cache, int cache_dtype,
+                             const float *gate_f, const float *A_log, const float *dt_bias,
+                             float gate_lower_bound, const float *beta, float *state,
+                             float scale, const float *out_gate, const float *norm_weight,
+                             float norm_eps, float *y, int M, int T, int H, int dk, int dv,
+                             int chunk, void *stream);
+
 /* kda_chunk_prefill with an explicit kernel (kda_prefill_kernel). */
 kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v, int qkv_dtype,
                                     const float *alpha, const float *beta, float *state,

@@ -178,7 +178,7 @@ kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v,
     const kda_status st =
         check_prefill(q, k, v, qkv_dtype, alpha, beta, state, o, M, T, H, dk, dv, chunk);
     if (st != KDA_OK) return st;
-    kda::PrefillArgs a;
+    kda::PrefillArgs a = {};
     a.q = q;
     a.k = k;
     a.v = v;
@@ -205,6 +205,60 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qk
                              void *stream) {
     return kda_chunk_prefill_config(q, k, v, qkv_dtype, alpha, beta, state, o, scale, M, T, H, dk,
                                     dv, chunk, KDA_PREFILL_AUTO, stream);
+}
+
+kda_status kda_prefill_layer(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
+                             int cache_dtype, const float *gate_f, const float *A_log,
+                             const float *dt_bias, float gate_lower_bound, const float *beta,
+                             float *state, float scale, const float *out_gate,
+                             const float *norm_weight, float norm_eps, float *y, int M, int T, int H,
+                             int dk, int dv, int chunk, void *stream) {
+    if (!x || !conv_w || !conv_cache || !gate_f || !A_log || !dt_bias || !beta || !state || !y ||
+        (out_gate && !norm_weight))
+        return KDA_ERR_INVALID_ARG;
+    if (M <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0 || chunk <= 0) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(x_dtype) || !valid_dtype(cache_dtype)) return KDA_ERR_INVALID_ARG;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim || chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (cache_dtype != x_dtype) return KDA_ERR_UNSUPPORTED;
+    if (M > 65535 || H > 65535) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_cache) || !aligned16(gate_f) ||
+        !aligned16(A_log) || !aligned16(dt_bias) || !aligned16(beta) || !aligned16(state) ||
+        !aligned16(y) || (out_gate && !aligned16(out_gate)) ||
+        (norm_weight && !aligned16(norm_weight)))
+        return KDA_ERR_ALIGNMENT;
+    const size_t D = (size_t)H * dk, tok = (size_t)M * T * H;
+    const size_t n_x = (size_t)M * T * 3 * D * dtype_bytes(x_dtype);
+    const size_t n_c = (size_t)M * 9 * D * dtype_bytes(cache_dtype);
+    const size_t n_f = tok * dk * 4, n_b = tok * 4, n_y = tok * dv * 4;
+    const size_t n_s = (size_t)M * H * dk * dv * 4;
+    const void *ins[4] = {x, gate_f, beta, out_gate};
+    const size_t ns[4] = {n_x, n_f, n_b, out_gate ? n_y : 0};
+    for (int i = 0; i < 4; ++i)
+        if (ins[i] && (overlap(y, n_y, ins[i], ns[i]) || overlap(state, n_s, ins[i], ns[i]) ||
+                       overlap(conv_cache, n_c, ins[i], ns[i])))
+            return KDA_ERR_INVALID_ARG;
+    if (overlap(y, n_y, state, n_s) || overlap(y, n_y, conv_cache, n_c) ||
+        overlap(state, n_s, conv_cache, n_c))
+        return KDA_ERR_INVALID_ARG;
+    kda::PrefillArgs a = {};
+    a.q = x;
+    a.alpha = gate_f;
+    a.beta = beta;
+    a.state = state;
+    a.o = y;
+    a.M = M;
+    a.T = T;
+    a.H = H;
+    a.scale = scale;
+    a.conv_w = conv_w;
+    a.cache = conv_cache;
+    a.A_log = A_log;
+    a.dt_bias = dt_bias;
+    a.gate_lb = gate_lower_bound;
+    a.out_gate = out_gate;
+    a.norm_w = norm_weight;
+    a.norm_eps = norm_eps;
+    return cuda_status(kda::launch_prefill_layer(a, x_dtype, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w,

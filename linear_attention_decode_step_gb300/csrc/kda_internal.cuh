@@ -36,13 +36,22 @@ struct DecodeArgs {
 
 // Arguments of one chunked prefill (layouts as documented in kda.h).
 struct PrefillArgs {
-    const void *q, *k, *v;  // [M, T, H, 128] post-conv (qkv dtype)
-    const float *alpha;     // [M, T, H, 128]
+    const void *q, *k, *v;  // [M, T, H, 128] post-conv (qkv dtype); the layer form: q = pre-conv x [M, T, 3, H*128]
+    const float *alpha;     // [M, T, H, 128]; the layer form: raw forget-gate input f
     const float *beta;      // [M, T, H]
     float *state;           // [M, H, 128, 128] in / out
     float *o;               // [M, T, H, 128]
     int M, T, H;
     float scale;
+    // the layer form (conv + SiLU, gate and optional gated RMSNorm fused in)
+    const float *conv_w;    // [3, H*128, 4]
+    void *cache;            // [M, 3, 3, H*128] (qkv dtype), in / out
+    const float *A_log;     // [H]
+    const float *dt_bias;   // [H*128]
+    float gate_lb;
+    const float *out_gate;  // [M, T, H, 128] or null (no norm)
+    const float *norm_w;    // [128]
+    float norm_eps;
 };
 
 // Chunked prefill on CUDA cores (64-token chunks, 16-token blocks).
@@ -50,6 +59,12 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, int qkv_dtype, cudaStream_
 
 // Chunked prefill on the tensor cores (tcgen05, TF32 operands, state in TMEM).
 cudaError_t launch_prefill_tc(const PrefillArgs &a, int qkv_dtype, cudaStream_t stream);
+
+// The tensor-core prefill of a whole KDA layer over a prompt: conv + SiLU of
+// the pre-conv x with the cache as left context (cache updated), the forget
+// gate from its raw input, the chunked recurrence and, if a.out_gate is set,
+// the gated RMSNorm on every output.
+cudaError_t launch_prefill_layer(const PrefillArgs &a, int x_dtype, cudaStream_t stream);
 
 // Reads and clears the tensor-core prefill's device error word.
 cudaError_t take_prefill_error(unsigned int *code);

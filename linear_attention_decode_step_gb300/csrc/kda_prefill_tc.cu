@@ -30,7 +30,9 @@
 // per-token log-decays, which stays inside FP32 for log(alpha) above about
 // -5.4 (the model's gate keeps it above -5; section 8.2.3 ties the -5 floor to
 // 16-token spans). The block of second-half rows against first-half columns
-// uses the second half's left factor and R0o = K e^{m_1 - G} <= 1 on the right.
+// uses the second half's left factor and R0o = K e^{m_1 - G} <= 1 on the right,
+// with its own exponent (a product of separately rounded factors would
+// underflow where the decay is strong).
 // Every factor of Kd, Qd, Kdec and the state decay is <= 1.
 //
 // Thread roles. "Token-channel" work (decay scan, norms, operand tiles): warp
@@ -101,7 +103,15 @@ constexpr uint32_t S_NORM = TILES;                 // [2][64 rows][LDN] partial 
 constexpr uint32_t S_XCH = S_NORM + 2 * 64 * LDN * 4;  // [3][128]: G_31, L_47, L_63 per channel
 constexpr uint32_t S_BETA = S_XCH + 3 * 128 * 4;
 constexpr uint32_t S_GAM = S_BETA + 64 * 4;        // [128] e^{G_63}
-constexpr uint32_t S_BAR = S_GAM + 128 * 4;        // 4 mbarriers
+// the layer form: raw q, k of the three tokens before each half
+// ([tensor][tap][channel]: xa = tokens 29-31 of this chunk, xb[2] = tokens
+// 61-63 of the previous chunk by chunk parity) and the q, k conv weights
+constexpr uint32_t S_XA = S_GAM + 128 * 4;
+constexpr uint32_t XB_F = 2 * 3 * 128;
+constexpr uint32_t S_XB = S_XA + XB_F * 4;
+constexpr uint32_t S_WQK = S_XB + 2 * XB_F * 4;    // [3][128] float4: q, k, v conv weights
+constexpr uint32_t S_BIAS = S_WQK + 3 * 128 * 16;  // [128] gate bias of the head
+constexpr uint32_t S_BAR = S_BIAS + 128 * 4;       // 4 mbarriers
 constexpr uint32_t S_SLOT = S_BAR + 4 * 8;
 constexpr uint32_t SMEM_BYTES = S_SLOT + 16;
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in shared memory");
@@ -191,19 +201,26 @@ struct QKA {
     typename Raw<TQ>::Q4 q[4], k[4];
     float4 al[4];
 };
-template <typename TQ>
+template <typename TQ, bool LAYER>
 __device__ __forceinline__ void load_qka(QKA<TQ> &R, const PrefillArgs &a, int m, int h, int t0,
                                          int c4) {
     using RW = Raw<TQ>;
     const TQ *q = static_cast<const TQ *>(a.q);
     const TQ *k = static_cast<const TQ *>(a.k);
+    const size_t D = (size_t)a.H * DK;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const int t = t0 + 8 * g;
         if (t < a.T) {
             const size_t base = (((size_t)m * a.T + t) * a.H + h) * DK + 4 * c4;
-            R.q[g] = RW::load4(q + base);
-            R.k[g] = RW::load4(k + base);
+            if (LAYER) {  // pre-conv x [M][T][3][D]: q is tensor 0, k tensor 1
+                const size_t xb = (((size_t)m * a.T + t) * 3) * D + (size_t)h * DK + 4 * c4;
+                R.q[g] = RW::load4(q + xb);
+                R.k[g] = RW::load4(q + xb + D);
+            } else {
+                R.q[g] = RW::load4(q + base);
+                R.k[g] = RW::load4(k + base);
+            }
             R.al[g] = __ldg(reinterpret_cast<const float4 *>(a.alpha + base));
         } else {
             R.q[g] = R.k[g] = typename RW::Q4{};
@@ -224,7 +241,40 @@ __device__ __forceinline__ void load_v(typename Raw<TQ>::V1 (&v)[16], const Pref
     }
 }
 
+// the layer form: raw pre-conv v of tokens t0 - 3 .. t0 + 15 at value channel
+// j (the cache supplies tokens before the sequence, tokens past T read 0) ...
 template <typename TQ>
+__device__ __forceinline__ void load_v19(typename Raw<TQ>::V1 (&raw)[19], const PrefillArgs &a, int m,
+                                         int h, int t0, int j) {
+    using RW = Raw<TQ>;
+    const TQ *x = static_cast<const TQ *>(a.q);
+    const TQ *cache = static_cast<const TQ *>(a.cache);
+    const size_t D = (size_t)a.H * DK;
+#pragma unroll
+    for (int i = 0; i < 19; ++i) {
+        const int t = t0 - 3 + i;
+        if (t < 0)  // the cache holds tokens -3, -2, -1 as taps 0, 1, 2
+            raw[i] = RW::load1(cache + ((size_t)m * 9 + 6 + (t + 3)) * D + (size_t)h * DK + j);
+        else if (t < a.T)
+            raw[i] = RW::load1(x + (((size_t)m * a.T + t) * 3 + 2) * D + (size_t)h * DK + j);
+        else
+            raw[i] = RW::zero1();
+    }
+}
+// ... and their conv (kernel 4) + SiLU; tokens past T give 0
+template <typename TQ>
+__device__ __forceinline__ void conv_v(float (&v)[16], const typename Raw<TQ>::V1 (&raw)[19], int t0,
+                                       int T, const float4 w) {
+    using RW = Raw<TQ>;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float pre = w.x * RW::widen1(raw[i]) + w.y * RW::widen1(raw[i + 1]) +
+                          w.z * RW::widen1(raw[i + 2]) + w.w * RW::widen1(raw[i + 3]);
+        v[i] = t0 + i < T ? __fdividef(pre, 1.0f + __expf(-pre)) : 0.f;
+    }
+}
+
+template <typename TQ, bool LAYER, bool NORM>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     float *sNorm = reinterpret_cast<float *>(sm + S_NORM);
@@ -238,6 +288,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     float *sX = reinterpret_cast<float *>(sm + T_X);
     float *sKst = reinterpret_cast<float *>(sm + T_KST);
     float *sO = reinterpret_cast<float *>(sm + T_O);
+    float *sXa = reinterpret_cast<float *>(sm + S_XA);
+    float *sXb = reinterpret_cast<float *>(sm + S_XB);
+    float4 *sWqk = reinterpret_cast<float4 *>(sm + S_WQK);
+    float *sBias = reinterpret_cast<float *>(sm + S_BIAS);
 
     const int h = blockIdx.x % a.H, m = blockIdx.x / a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -278,8 +332,30 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     using RW = Raw<TQ>;
     QKA<TQ> R;
     float beta_n = 0.f;
-    load_qka<TQ>(R, a, m, h, r0, c4);
+    load_qka<TQ, LAYER>(R, a, m, h, r0, c4);
     if (tid < C) beta_n = tid < T ? __ldg(a.beta + ((size_t)m * T + tid) * a.H + h) : 0.f;
+
+    // the layer form: gate constants, conv weights, the cache as the tokens
+    // before the first chunk, and the raw q, k before the second half
+    const size_t D = (size_t)a.H * DK;
+    if (LAYER) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
+        if (tid < 3 * DK) sWqk[tid] = __ldg(w4 + (size_t)(tid >> 7) * D + (size_t)h * DK + (tid & 127));
+        if (tid < DK) sBias[tid] = __ldg(a.dt_bias + (size_t)h * DK + tid);
+        const TQ *cache = static_cast<const TQ *>(a.cache);
+        for (int i = tid; i < 2 * 3 * DK; i += NT) {  // xb[1][X][tap][c] = cache[m][X][tap][h, c]
+            const int X = i / (3 * DK), tap = (i / DK) % 3, c = i % DK;
+            sXb[XB_F + i] = RW::widen1(RW::load1(cache + ((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c));
+        }
+        if (rh == 0 && rr >= 5) {  // tokens 29-31 of chunk 0 (lanes rr = 5, 6, 7 of g = 3)
+            float xq[4], xk[4];
+            RW::widen4(R.q[3], xq);
+            RW::widen4(R.k[3], xk);
+            *reinterpret_cast<float4 *>(sXa + (0 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xq[0], xq[1], xq[2], xq[3]);
+            *reinterpret_cast<float4 *>(sXa + (1 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xk[0], xk[1], xk[2], xk[3]);
+        }
+        __syncthreads();
+    }
 
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
     const uint32_t id96 = umma::instr_desc(128, 96, umma::kFmtTF32);
@@ -295,10 +371,77 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         for (int g = 0; g < 4; ++g) {
             RW::widen4(R.q[g], qf[g]);
             RW::widen4(R.k[g], kf[g]);
-            G[g][0] = lg2(R.al[g].x);
-            G[g][1] = lg2(R.al[g].y);
-            G[g][2] = lg2(R.al[g].z);
-            G[g][3] = lg2(R.al[g].w);
+        }
+        if (LAYER) {
+            const int cidx = c0 / C;
+            // tokens 61-63 of this chunk, for the next chunk's first half
+            if (rh == 1 && rr >= 5) {
+                float *xb = sXb + (cidx & 1) * XB_F;
+                *reinterpret_cast<float4 *>(xb + (0 * 3 + rr - 5) * DK + 4 * c4) =
+                    make_float4(qf[3][0], qf[3][1], qf[3][2], qf[3][3]);
+                *reinterpret_cast<float4 *>(xb + (1 * 3 + rr - 5) * DK + 4 * c4) =
+                    make_float4(kf[3][0], kf[3][1], kf[3][2], kf[3][3]);
+            }
+            // forget gate in log2 units: lb sigmoid(e^A (f + b)) / ln 2
+            const float eA = __expf(__ldg(a.A_log + h));
+            const float lbl2 = a.gate_lb * 1.4426950408889634f;
+            const float4 b4 = *reinterpret_cast<const float4 *>(sBias + 4 * c4);
+            const float bias[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int t = c0 + 32 * rh + 8 * g + rr;
+                const float f4[4] = {R.al[g].x, R.al[g].y, R.al[g].z, R.al[g].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float z = eA * (f4[e] + bias[e]);
+                    G[g][e] = t < T ? __fdividef(lbl2, 1.0f + __expf(-z)) : 0.f;
+                }
+            }
+            // conv + SiLU, token groups from last to first (each reads the raw
+            // values of the group before it): token 8 g + rr - kk sits in lane
+            // rr - kk of group g, or in lane rr - kk + 8 of group g - 1, or (first
+            // group) in the buffer of the three tokens before the half, at tap
+            // rr - kk + 3
+            const float *xp = rh ? sXa : sXb + ((cidx + 1) & 1) * XB_F;
+#pragma unroll
+            for (int g = 3; g >= 0; --g) {
+                const int t = c0 + 32 * rh + 8 * g + rr;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float wq3[3], wk3[3];  // tokens t - 1, t - 2, t - 3
+#pragma unroll
+                    for (int kk = 1; kk <= 3; ++kk) {
+                        const int src = 8 * qq + ((rr - kk) & 7);
+                        const float aq = __shfl_sync(0xffffffffu, qf[g][e], src);
+                        const float ak = __shfl_sync(0xffffffffu, kf[g][e], src);
+                        float bq, bk;
+                        if (g > 0) {
+                            bq = __shfl_sync(0xffffffffu, qf[g > 0 ? g - 1 : 0][e], src);
+                            bk = __shfl_sync(0xffffffffu, kf[g > 0 ? g - 1 : 0][e], src);
+                        } else {
+                            const int tap = rr - kk + 3 < 2 ? rr - kk + 3 : 2;  // used only when rr < kk
+                            bq = xp[(0 * 3 + tap) * DK + 4 * c4 + e];
+                            bk = xp[(1 * 3 + tap) * DK + 4 * c4 + e];
+                        }
+                        wq3[kk - 1] = rr >= kk ? aq : bq;
+                        wk3[kk - 1] = rr >= kk ? ak : bk;
+                    }
+                    const float4 wq = sWqk[4 * c4 + e], wk = sWqk[DK + 4 * c4 + e];
+                    const float pre_q = wq.x * wq3[2] + wq.y * wq3[1] + wq.z * wq3[0] + wq.w * qf[g][e];
+                    const float pre_k = wk.x * wk3[2] + wk.y * wk3[1] + wk.z * wk3[0] + wk.w * kf[g][e];
+                    const bool live = t < T;  // tokens past T stay out of the chunk
+                    qf[g][e] = live ? __fdividef(pre_q, 1.0f + __expf(-pre_q)) : 0.f;
+                    kf[g][e] = live ? __fdividef(pre_k, 1.0f + __expf(-pre_k)) : 0.f;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                G[g][0] = lg2(R.al[g].x);
+                G[g][1] = lg2(R.al[g].y);
+                G[g][2] = lg2(R.al[g].z);
+                G[g][3] = lg2(R.al[g].w);
+            }
         }
         float carry[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -366,20 +509,21 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             rk[g] = 1.0f / sqrtf(ka.x + ka.y + ka.z + ka.w + kb.x + kb.y + kb.z + kb.w + kL2Eps);
         }
         // per-channel factors (log2 units):
-        //   half 0: u = e^{G - G_15};  R0o = R e^{G_31 + L_47 - G_15};
+        //   half 0: u = e^{G - G_15};  R0o = K e^{m_1 - G} with m_1 = G_31 + L_47
+        //           (its own exponent: R e^{m_1 - m_0} would lose it to underflow
+        //           of e^{m_1 - m_0} when the decay is strong);
         //           Kd = L e^{G_15};   Kdec = R e^{G_31 + L_63 - G_15}
         //   half 1: u = e^{L - L_47};  Kd = L e^{G_31 + L_47};  Kdec = R e^{L_63 - L_47}
-        float fo[4], em[4], ed[4];
+        float m1a[4], em[4], ed[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float g31 = sXch[4 * c4 + e], l47 = sXch[128 + 4 * c4 + e];
             const float l63 = sXch[256 + 4 * c4 + e];
+            m1a[e] = g31 + l47;
             if (rh == 0) {
-                fo[e] = ex2(g31 + l47 - mid[e]);
                 em[e] = ex2(mid[e]);
                 ed[e] = ex2(g31 + l63 - mid[e]);
             } else {
-                fo[e] = 0.f;
                 em[e] = ex2(g31 + l47);
                 ed[e] = ex2(l63 - l47);
             }
@@ -409,9 +553,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             st_tile4(sm + T_LA, rowL, c4, KB128, Lk[g][0], Lk[g][1], Lk[g][2], Lk[g][3]);
             st_tile4(sm + T_LA, rowLq, c4, KB128, Lq[g][0], Lq[g][1], Lq[g][2], Lq[g][3]);
             st_tile4(sm + T_RB, r, c4, KB128, Rk[g][0], Rk[g][1], Rk[g][2], Rk[g][3]);
-            if (rh == 0)
-                st_tile4(sm + T_RB, 64 + r, c4, KB128, Rk[g][0] * fo[0], Rk[g][1] * fo[1],
-                         Rk[g][2] * fo[2], Rk[g][3] * fo[3]);
+            if (rh == 0) {
+                float Ro[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Ro[e] = kf[g][e] * rk[g] * ex2(m1a[e] - G[g][e]);
+                st_tile4(sm + T_RB, 64 + r, c4, KB128, Ro[0], Ro[1], Ro[2], Ro[3]);
+            }
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
@@ -489,7 +636,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         __syncthreads();
         // the next chunk's q, k, alpha (the registers of this one are consumed)
-        if (c0 + C < T) load_qka<TQ>(R, a, m, h, c0 + C + r0, c4);
+        if (c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
         // Kdec^T tile (row = key channel c, K = token): 16-byte row segments,
         // 8 consecutive channels per quarter-warp (one core matrix)
 #pragma unroll
@@ -516,8 +663,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
         // (runs on CUDA cores while MMA3 is on the tensor cores; v of this
         // chunk is loaded meanwhile)
-        typename RW::V1 vr[16];
-        load_v<TQ>(vr, a, m, h, c0 + 16 * hq, j);
+        typename RW::V1 vr[LAYER ? 19 : 16];
+        if constexpr (LAYER) load_v19<TQ>(vr, a, m, h, c0 + 16 * hq, j);
+        else load_v<TQ>(vr, a, m, h, c0 + 16 * hq, j);
         // 5a. diagonal 16 x 16 blocks, one lane per column: T_bb = (I + A_bb)^-1
         if (warp < 2) {
             const int b = 2 * warp + (lane >> 4), jj = lane & 15, j0 = 16 * b;
@@ -601,11 +749,18 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         umma::fence_after_sync();
         {
+            float vf[16];
+            if constexpr (LAYER) {
+                conv_v<TQ>(vf, vr, c0 + 16 * hq, T, sWqk[2 * DK + j]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) vf[e] = RW::widen1(vr[e]);
+            }
             float y[16];  // tokens 16 hq .. 16 hq + 15
             umma::ld_x16(tq + TM_D3 + 16 * hq, y);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) y[e] = tf32r(RW::widen1(vr[e]) - y[e]);
+            for (int e = 0; e < 16; ++e) y[e] = tf32r(vf[e] - y[e]);
             umma::st_x16(tq + TM_Z + 16 * hq, y);
         }
         {  // S^T[j][c] *= e^{G63_c}
@@ -617,6 +772,14 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             umma::st_x32(tq + TM_S + 32 * hq, s32);
         }
         umma::wait_st();
+        // the layer form: raw q, k of tokens 29-31 of the next chunk (loaded in phase 4)
+        if (LAYER && rh == 0 && rr >= 5 && c0 + C < T) {
+            float xq[4], xk[4];
+            RW::widen4(R.q[3], xq);
+            RW::widen4(R.k[3], xk);
+            *reinterpret_cast<float4 *>(sXa + (0 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xq[0], xq[1], xq[2], xq[3]);
+            *reinterpret_cast<float4 *>(sXa + (1 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xk[0], xk[1], xk[2], xk[3]);
+        }
 
         umma::fence_before_sync();
         __syncthreads();
@@ -657,6 +820,28 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
 #pragma unroll
             for (int e = 0; e < 16; ++e) sO[(16 * hq + e) * DK + j] = a.scale * o16[e];
         }
+        if (NORM) {  // y = o / sqrt(mean o^2 + eps) * w * sigmoid(gate), warp w: rows 4 w .. 4 w + 3
+            __syncthreads();
+            const float4 nw = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * warp + i;
+                float4 *row = reinterpret_cast<float4 *>(sO + t * DK) + lane;
+                float4 o4 = *row;
+                float ss = o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float rn = rsqrtf(ss * (1.0f / DK) + a.norm_eps);
+                float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c0 + t < T)
+                    g4 = __ldg(reinterpret_cast<const float4 *>(a.out_gate + (((size_t)m * T + c0 + t) * a.H + h) * DK) + lane);
+                o4.x = o4.x * rn * nw.x / (1.0f + __expf(-g4.x));
+                o4.y = o4.y * rn * nw.y / (1.0f + __expf(-g4.y));
+                o4.z = o4.z * rn * nw.z / (1.0f + __expf(-g4.z));
+                o4.w = o4.w * rn * nw.w / (1.0f + __expf(-g4.w));
+                *row = o4;
+            }
+        }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         if (warp == 0) ptx::named_bar_sync(kBarOut, NT);
@@ -683,28 +868,50 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             for (int e = 0; e < 8; ++e) state[(size_t)(c + e) * DK + j] = v8[e];
         }
     }
+    if (LAYER && ok && tid < 3 * DK) {  // conv cache <- the last three inputs of (cache, x)
+        TQ *cache = static_cast<TQ *>(a.cache);
+        const TQ *x = static_cast<const TQ *>(a.q);
+        const int X = tid / DK, c = tid % DK;
+        typename RW::V1 nv[3];
+#pragma unroll
+        for (int tap = 0; tap < 3; ++tap) {
+            const int t = T - 3 + tap;
+            nv[tap] = t >= 0 ? RW::load1(x + (((size_t)m * T + t) * 3 + X) * D + (size_t)h * DK + c)
+                             : RW::load1(cache + ((size_t)m * 9 + 3 * X + t + 3) * D + (size_t)h * DK + c);
+        }
+#pragma unroll
+        for (int tap = 0; tap < 3; ++tap)
+            reinterpret_cast<typename RW::V1 *>(cache)[((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c] = nv[tap];
+    }
     if (warp == 0) ptx::bulk_wait_all();  // O copies complete before the CTA's shared memory goes
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tb, TM_COLS);
 }
 
+template <typename TQ, bool LAYER, bool NORM>
+cudaError_t launch_tc_typed(const PrefillArgs &a, cudaStream_t stream) {
+    auto kernel = kda_prefill_tc_kernel<TQ, LAYER, NORM>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3(a.M * a.H), NT, SMEM_BYTES, stream>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, int qkv_dtype, cudaStream_t stream) {
-    const dim3 grid(a.M * a.H);
-    if (qkv_dtype == KDA_BF16) {
-        cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel<__nv_bfloat16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        kda_prefill_tc_kernel<__nv_bfloat16><<<grid, NT, SMEM_BYTES, stream>>>(a);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel<float>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        kda_prefill_tc_kernel<float><<<grid, NT, SMEM_BYTES, stream>>>(a);
+    if (qkv_dtype == KDA_BF16) return launch_tc_typed<__nv_bfloat16, false, false>(a, stream);
+    return launch_tc_typed<float, false, false>(a, stream);
+}
+
+cudaError_t launch_prefill_layer(const PrefillArgs &a, int x_dtype, cudaStream_t stream) {
+    if (x_dtype == KDA_BF16) {
+        if (a.out_gate) return launch_tc_typed<__nv_bfloat16, true, true>(a, stream);
+        return launch_tc_typed<__nv_bfloat16, true, false>(a, stream);
     }
-    return cudaGetLastError();
+    if (a.out_gate) return launch_tc_typed<float, true, true>(a, stream);
+    return launch_tc_typed<float, true, false>(a, stream);
 }
 
 cudaError_t take_prefill_error(unsigned int *code) {

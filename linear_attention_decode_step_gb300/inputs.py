@@ -36,6 +36,7 @@ __all__ = [
     "layer_seed",
     "gate_norm_inputs",
     "stack_tokens",
+    "prefill_layer_problem",
 ]
 
 
@@ -158,3 +159,34 @@ def stack_tokens(layer: dict) -> dict:
         "alpha": np.ascontiguousarray(np.stack(layer["alpha"], axis=1)),
         "beta": np.ascontiguousarray(np.stack(layer["beta"], axis=1)),
     }
+
+
+def prefill_layer_problem(seed: int, M: int, T: int, H: int = 64, d: int = 128) -> dict:
+    """Inputs of a KDA layer over a prompt of T tokens: pre-conv x ~ N(0, 1)
+    [M, T, 3, D] and conv cache ~ N(0, 1) [M, 3, 3, D] as BF16 bits (x_bits,
+    cache_bits; widened x_f32, cache_f32), conv_w ~ N(0, 0.5^2) [3, D, 4],
+    the raw gate input f ~ N(0, 1) [M, T, H, d], A_log ~ U(-1, 1) [H],
+    dt_bias ~ N(0, 1) [H*d], beta = sigmoid(N(0, 1)) [M, T, H], S0 ~
+    N(0, 0.1^2) rounded to BF16 [M, H, d, d], the output gate ~ N(0, 1)
+    [M, T, H, d] and the RMSNorm weight ~ N(1, 0.1^2) [d]. Draw order as
+    listed."""
+    rng = np.random.default_rng(seed)
+    D = H * d
+    x_bits = bf16_bits(rng.standard_normal((M, T, 3, D), dtype=np.float32))
+    cache_bits = bf16_bits(rng.standard_normal((M, 3, 3, D), dtype=np.float32))
+    conv_w = rng.standard_normal((3, D, 4), dtype=np.float32)
+    conv_w *= np.float32(0.5)
+    f = rng.standard_normal((M, T, H, d), dtype=np.float32)
+    A_log = rng.uniform(-1.0, 1.0, H).astype(np.float32)
+    dt_bias = rng.standard_normal(H * d).astype(np.float32)
+    beta = _sigmoid32(rng.standard_normal((M, T, H)))
+    S0 = rng.standard_normal((M, H, d, d), dtype=np.float32)
+    S0 *= np.float32(0.1)
+    S0 = bf16_widen(bf16_bits(S0))
+    out_gate = rng.standard_normal((M, T, H, d), dtype=np.float32)
+    norm_w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    return {"M": M, "T": T, "H": H, "d": d,
+            "x_bits": x_bits, "x_f32": bf16_widen(x_bits),
+            "cache_bits": cache_bits, "cache_f32": bf16_widen(cache_bits),
+            "conv_w": conv_w, "f": f, "A_log": A_log, "dt_bias": dt_bias, "beta": beta,
+            "S0": np.ascontiguousarray(S0), "out_gate": out_gate, "norm_w": norm_w}

@@ -58,6 +58,8 @@ _SIGNATURES = {
                                _I, _I, _I, _I, _V], _I),
     "kda_decode_tokens": ([_V, _I, _V, _V, _I, _V, _V, _V, _I, _F, _V,
                            _I, _I, _I, _I, _I, _V], _I),
+    "kda_prefill_layer": ([_V, _I, _V, _V, _I, _V, _V, _V, _F, _V, _V, _F, _V, _V, _F, _V,
+                           _I, _I, _I, _I, _I, _I, _V], _I),
     "kda_chunk_prefill": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I, _V], _I),
     "kda_chunk_prefill_config": ([_V, _V, _V, _I, _V, _V, _V, _V, _F, _I, _I, _I, _I, _I, _I,
                                   _I, _V], _I),
@@ -274,3 +276,30 @@ def kda_chunk_prefill_config(q, k, v, alpha, beta, state, o=None, scale=1.0, chu
                                         int(kernel), _stream(stream))
     _check("kda_chunk_prefill_config", st)
     return o
+
+
+def kda_prefill_layer(x, conv_w, conv_cache, gate_f, A_log, dt_bias, beta, state, y=None,
+                      scale=1.0, gate_lower_bound=-5.0, out_gate=None, norm_weight=None,
+                      norm_eps=1e-5, chunk=64, stream=None):
+    """A KDA layer over a prompt (see kda.h): x [M,T,3,H*128] pre-conv (bf16|f32),
+    conv_cache [M,3,3,H*128] (same dtype, updated in place), gate_f [M,T,H,128]
+    f32 raw gate input, beta [M,T,H] f32, state [M,H,128,128] f32 updated in
+    place; with out_gate and norm_weight the gated RMSNorm is applied.
+    Returns y [M,T,H,128] f32."""
+    M, T, three, D = x.shape
+    H = state.shape[1]
+    dk, dv = state.shape[2], state.shape[3]
+    if y is None:
+        y = torch.empty((M, T, H, dv), dtype=torch.float32, device=x.device)
+    og = _dev(out_gate, "out_gate", torch.float32) if out_gate is not None else None
+    nw = _dev(norm_weight, "norm_weight", torch.float32) if norm_weight is not None else None
+    st = lib().kda_prefill_layer(
+        _dev(x, "x"), _dtype_code(x), _dev(conv_w, "conv_w", torch.float32),
+        _dev(conv_cache, "conv_cache"), _dtype_code(conv_cache),
+        _dev(gate_f, "gate_f", torch.float32), _dev(A_log, "A_log", torch.float32),
+        _dev(dt_bias, "dt_bias", torch.float32), float(gate_lower_bound),
+        _dev(beta, "beta", torch.float32), _dev(state, "state", torch.float32), float(scale),
+        og, nw, float(norm_eps), _dev(y, "y", torch.float32), M, T, H, dk, dv, int(chunk),
+        _stream(stream))
+    _check("kda_prefill_layer", st)
+    return y

@@ -37,6 +37,7 @@ __all__ = [
     "gated_rmsnorm",
     "decode_step_fused",
     "decode_tokens",
+    "prefill_layer",
     "L2_EPS",
     "GATE_LOWER_BOUND",
     "NORM_EPS",
@@ -210,6 +211,25 @@ def decode_tokens(x, w, cache, alpha, beta, S0, scale=1.0, eps=L2_EPS):
     for t in range(T):
         o[:, t], S, c = decode_step(x[:, t], w, c, alpha[:, t], beta[:, t], S,
                                     scale=scale, eps=eps)
+    return o, S, c
+
+
+def prefill_layer(x, w, cache, f, A_log, dt_bias, beta, S0, scale=1.0, out_gate=None,
+                  norm_w=None, lb=GATE_LOWER_BOUND, eps=L2_EPS, norm_eps=NORM_EPS):
+    """A KDA layer over a prompt of T tokens ("GLM-5.3 deep dive" 8.2.4):
+    the forget gate turns the raw gate input f into alpha (8.2.3), then the T
+    tokens go through the decode steps in order (short conv + SiLU with the
+    cache as left context, L2 norm, Eq. 1, read; 8.2.5 states that the chunked
+    form reaches the same result), then, if out_gate is given, the gated
+    RMSNorm on each token's output (8.2.4 step 7).
+
+    x [M,T,3,D]; w [3,D,4]; cache [M,3,3,D]; f [M,T,H,d]; A_log [H];
+    dt_bias [H*d]; beta [M,T,H]; S0 [M,H,d,d]; out_gate [M,T,H,d] or None
+    -> (y or o [M,T,H,d], S, cache)."""
+    alpha = forget_gate(f, A_log, dt_bias, lb)
+    o, S, c = decode_tokens(x, w, cache, alpha, beta, S0, scale=scale, eps=eps)
+    if out_gate is not None:
+        o = gated_rmsnorm(o, out_gate, norm_w, norm_eps)
     return o, S, c
 
 

@@ -158,3 +158,24 @@ def _tokens_call(K, **over):
 ])
 def test_tokens_rejects(K, over, status):
     assert _tokens_call(K, **over) == status
+
+
+def _layer_call(K, **over):
+    a = dict(x=BASE, xd=K.KDA_BF16, w=BASE + GAP, cache=BASE + 2 * GAP, cd=K.KDA_BF16,
+             f=BASE + 3 * GAP, A=BASE + 4 * GAP, bias=BASE + 5 * GAP, lb=-5.0,
+             beta=BASE + 6 * GAP, state=BASE + 7 * GAP, scale=1.0, og=None, nw=None,
+             neps=1e-5, y=BASE + 8 * GAP, M=4, T=4096, H=64, dk=128, dv=128, chunk=64)
+    a.update(over)
+    return K.lib().kda_prefill_layer(a["x"], a["xd"], a["w"], a["cache"], a["cd"], a["f"], a["A"],
+                                     a["bias"], a["lb"], a["beta"], a["state"], a["scale"],
+                                     a["og"], a["nw"], a["neps"], a["y"], a["M"], a["T"], a["H"],
+                                     a["dk"], a["dv"], a["chunk"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(x=None), 1), (dict(f=None), 1), (dict(A=None), 1), (dict(T=0), 1), (dict(chunk=32), 2),
+    (dict(dk=64), 2), (dict(cd=0), 2), (dict(og=BASE + 9 * GAP), 1),  # out_gate without weight
+    (dict(f=BASE + 3 * GAP + 4), 3), (dict(state=BASE + 2 * GAP), 1),  # state aliases the cache
+])
+def test_layer_rejects(K, over, status):
+    assert _layer_call(K, **over) == status

@@ -75,3 +75,26 @@ def test_tokens_split_anywhere():
     np.testing.assert_allclose(np.concatenate([oa, ob], axis=1), o, rtol=0, atol=0)
     np.testing.assert_array_equal(Sb, S)
     np.testing.assert_array_equal(cb, c)
+
+
+def test_prefill_layer_is_gate_then_tokens_then_norm():
+    """The layer over a prompt composes pinned pieces: for one token it is the
+    fused decode step; for T tokens, the gate applied token-wise then the
+    multi-token decode, then the norm."""
+    rng = np.random.default_rng(740)
+    M, T, H, d = 2, 5, 2, 4
+    x, w, cache, _, b, S0 = _problem(rng, M, T, H, d)
+    f = rng.standard_normal((M, T, H, d))
+    A = rng.uniform(-1, 1, H)
+    bias = rng.standard_normal(H * d)
+    og = rng.standard_normal((M, T, H, d))
+    nw = 1 + 0.1 * rng.standard_normal(d)
+    y, S, c = oracle.prefill_layer(x, w, cache, f, A, bias, b, S0, scale=0.5, out_gate=og, norm_w=nw)
+    # token by token through the fused decode step
+    Sr, cr = S0, cache
+    for t in range(T):
+        yt, Sr, cr = oracle.decode_step_fused(x[:, t], w, cr, f[:, t], A, bias, b[:, t], Sr,
+                                              scale=0.5, out_gate=og[:, t], norm_w=nw)
+        np.testing.assert_allclose(y[:, t], yt, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S, Sr, rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(c, cr)

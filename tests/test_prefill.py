@@ -139,3 +139,19 @@ def test_config4_full_size_sampled_heads(K, kernel):
     for (m, h), orf, srf in zip(heads, o_ref, S_ref):
         assert rel_err(o[m, :, h], orf) <= TOL, ((m, h), rel_err(o[m, :, h], orf))
         assert rel_err(S[m, h], srf) <= TOL, ((m, h), rel_err(S[m, h], srf))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_mixed_channel_decay_from_the_gate(K, kernel):
+    """alpha from the model's forget gate (section 8.2.3): per channel some
+    decays sit at the e^-5 floor and others near 1 inside one chunk, so the
+    cross-half decay factor of a fast channel underflows while its true
+    products with neighbouring tokens do not."""
+    p = inputs.prefill_problem(4500, M=1, T=200, H=3)
+    gn = inputs.gate_norm_inputs(4501, M=1, H=3, d=128, T=200)
+    f = np.stack(gn["f"], axis=1)  # [M, T, H, d]
+    p["alpha"] = oracle.forget_gate(f, gn["A_log"], gn["dt_bias"]).astype(np.float32)
+    o, S = _run(K, p, kernel=kernel)
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(o, o_ref) <= TOL, rel_err(o, o_ref)
+    assert rel_err(S, S_ref) <= TOL
