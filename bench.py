@@ -468,6 +468,44 @@ def time_prefill(torch, kda, inputs, M, T, K, W, kernel=0):
     return e0.elapsed_time(e1) / K
 
 
+def time_prefill_layer(torch, kda, inputs, M, T, K, W, norm=True):
+    """K calls of kda_prefill_layer (conv + gate + chunked recurrence + gated
+    RMSNorm) on one (M, T, 64-head) prompt resident on the GPU; state and
+    cache updated in place. Returns ms per call."""
+    p = inputs.prefill_layer_problem(inputs.layer_seed(4, 2), M=M, T=T, H=H)
+    dev = torch.device("cuda")
+    bf = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    x, cache = bf(p["x_bits"]), bf(p["cache_bits"])
+    t = {n: torch.from_numpy(p[n]).to(dev) for n in ("conv_w", "f", "A_log", "dt_bias", "beta",
+                                                   "S0", "out_gate", "norm_w")}
+    y = torch.empty((M, T, H, DH), dtype=torch.float32, device=dev)
+    del p
+    run = lambda: kda.kda_prefill_layer(x, t["conv_w"], cache, t["f"], t["A_log"], t["dt_bias"],
+                                        t["beta"], t["S0"], y,
+                                        out_gate=t["out_gate"] if norm else None,
+                                        norm_weight=t["norm_w"] if norm else None)
+    for _ in range(W):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    if kda.kda_device_error() != kda.KDA_OK:
+        raise RuntimeError("prefill layer reported a device-side timeout")
+    return e0.elapsed_time(e1) / K
+
+
+def prefill_layer_bytes(M, T, H, x_bytes=2, norm=True):
+    """Algorithmic bytes of one layer prefill: pre-conv x, gate input f, beta
+    (and the output gate) in, y out, state and conv cache read and written."""
+    tok = M * T * H
+    per = 3 * x_bytes + 4 + 4 + (4 if norm else 0)
+    return tok * DH * per + tok * 4 + 2 * M * H * DH * DH * 4 + 2 * M * 9 * H * DH * x_bytes
+
+
 def prefill_summary(ms, M, T, peak_hbm, peak_bf16, kernel_name):
     gb = prefill_bytes(M, T, H) / 1e9
     tflop = prefill_flops(M, T, H) / 1e12
@@ -696,6 +734,16 @@ def own_arm(args, rank: int, world: int, local_rank: int):
         pms = time_prefill(torch, kda, inputs, 4, 4096, min(args.steps, 20), 3,
                            kernel=args.prefill_kernel)
         line["prefill"] = prefill_summary(pms, 4, 4096, peak, measured_bf16(), pk)
+        lms = time_prefill_layer(torch, kda, inputs, 4, 4096, min(args.steps, 20), 3)
+        lgb = prefill_layer_bytes(4, 4096, H) / 1e9
+        line["prefill_layer"] = {
+            "workload": "kda_prefill_layer: the same prompt (M=4 x T=4096 x 64 heads) as a whole "
+                        "layer: pre-conv BF16 x with the conv cache, raw gate input, chunked "
+                        "recurrence, gated RMSNorm",
+            "kernel": "kda_prefill_tc_kernel<bf16, layer, norm>", "ms": lms,
+            "tokens_per_s": 4 * 4096 / (lms * 1e-3), "gb_s": lgb / (lms * 1e-3),
+            "frac_of_measured_hbm": lgb / (lms * 1e-3) / peak,
+            "algorithmic_bytes": lgb * 1e9}
     if not args.no_tokens:
         mhz = clk.get("sm_mhz") if isinstance(clk, dict) else None
         rows = [tokens_summary(time_tokens(torch, kda, inputs, M_, T, args.state_dtype, 30, 3),
@@ -745,6 +793,8 @@ def main():
     ap.add_argument("--tokens-T", type=int, default=4)
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill (with --prefill-M/--prefill-T), one JSON line")
+    ap.add_argument("--prefill-layer", action="store_true",
+                    help="with --prefill-only: time kda_prefill_layer instead")
     ap.add_argument("--prefill-M", type=int, default=4)
     ap.add_argument("--prefill-T", type=int, default=4096)
     ap.add_argument("--sweep", action="store_true",
@@ -779,9 +829,18 @@ def main():
         from linear_attention_decode_step_gb300 import build, inputs, kda
         build.build()
         torch.cuda.set_device(0)
+        peak, _ = measured_peak()
+        if args.prefill_layer:
+            lms = time_prefill_layer(torch, kda, inputs, args.prefill_M, args.prefill_T,
+                                     args.steps, args.warmup)
+            lgb = prefill_layer_bytes(args.prefill_M, args.prefill_T, H) / 1e9
+            print(json.dumps({"kernel": "kda_prefill_layer", "M": args.prefill_M,
+                              "T": args.prefill_T, "ms": lms,
+                              "tokens_per_s": args.prefill_M * args.prefill_T / (lms * 1e-3),
+                              "frac_of_measured_hbm": lgb / (lms * 1e-3) / peak}))
+            return
         pms = time_prefill(torch, kda, inputs, args.prefill_M, args.prefill_T, args.steps,
                            args.warmup, kernel=args.prefill_kernel)
-        peak, _ = measured_peak()
         print(json.dumps(prefill_summary(pms, args.prefill_M, args.prefill_T, peak,
                                          measured_bf16(), "kernel %d" % args.prefill_kernel)))
         return

@@ -91,9 +91,8 @@ constexpr uint32_t T_A = T_P + 64 * KB64;          // A (plain [64][68] FP32)
 constexpr int LDA = 68;
 constexpr uint32_t T_T = T_A + 64 * LDA * 4;       // T = (I + A)^-1 (plain [64][68] FP32)
 constexpr uint32_t T_X = T_T + 64 * LDA * 4;       // scratch: up to 3 blocks of 16 x 16
-constexpr int LDK = 132;                           // Kdec staging row: 128 + 4
-constexpr uint32_t T_KST = T_X + 3 * 256 * 4;      // Kdec, token-major staging [64][LDK]
-constexpr uint32_t PH2_END = T_KST + 64 * LDK * 4;
+constexpr uint32_t T_V = T_X + 3 * 256 * 4;        // v of the chunk, token-major [64][128] (bulk copies)
+constexpr uint32_t PH2_END = T_V + 64 * DK * 4;
 constexpr uint32_t T_O = 0;                        // O staging [64][128] (phase 7, KQ is dead)
 static_assert(T_A >= PH1_END, "A and P are written while nothing reads phase-1 tiles");
 constexpr uint32_t TILES = PH2_END > PH1_END ? PH2_END : PH1_END;
@@ -111,14 +110,17 @@ constexpr uint32_t XB_F = 2 * 3 * 128;
 constexpr uint32_t S_XB = S_XA + XB_F * 4;
 constexpr uint32_t S_WQK = S_XB + 2 * XB_F * 4;    // [3][128] float4: q, k, v conv weights
 constexpr uint32_t S_BIAS = S_WQK + 3 * 128 * 16;  // [128] gate bias of the head
-constexpr uint32_t S_BAR = S_BIAS + 128 * 4;       // 4 mbarriers
-constexpr uint32_t S_SLOT = S_BAR + 4 * 8;
+constexpr uint32_t S_VC = S_BIAS + 128 * 4;        // [2][3][128] raw v of the 3 tokens before a chunk
+constexpr uint32_t S_BAR = S_VC + 2 * 3 * 128 * 4; // 5 mbarriers
+constexpr uint32_t S_SLOT = S_BAR + 6 * 8;
 constexpr uint32_t SMEM_BYTES = S_SLOT + 16;
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in shared memory");
 
 // the thread that issues every MMA: lane 0 of the last warp (free of the
 // phase-specific work that warps 0-1 carry in the inverse)
 constexpr int kIssuer = NT - 32;
+// the warp that issues the bulk copies of v
+constexpr int kVWarp = NT / 32 - 2;
 // named barriers (0 is __syncthreads): the issuer waits for all threads,
 // the others only signal and move on
 constexpr uint32_t kBarMma1 = 1, kBarMma3 = 2, kBarOut = 3;
@@ -228,52 +230,6 @@ __device__ __forceinline__ void load_qka(QKA<TQ> &R, const PrefillArgs &a, int m
         }
     }
 }
-// v of 16 tokens t0 .. t0 + 15 at value channel j (tensor-memory mapping)
-template <typename TQ>
-__device__ __forceinline__ void load_v(typename Raw<TQ>::V1 (&v)[16], const PrefillArgs &a, int m,
-                                       int h, int t0, int j) {
-    using RW = Raw<TQ>;
-    const TQ *vp = static_cast<const TQ *>(a.v);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int t = t0 + i;
-        v[i] = t < a.T ? RW::load1(vp + (((size_t)m * a.T + t) * a.H + h) * DK + j) : RW::zero1();
-    }
-}
-
-// the layer form: raw pre-conv v of tokens t0 - 3 .. t0 + 15 at value channel
-// j (the cache supplies tokens before the sequence, tokens past T read 0) ...
-template <typename TQ>
-__device__ __forceinline__ void load_v19(typename Raw<TQ>::V1 (&raw)[19], const PrefillArgs &a, int m,
-                                         int h, int t0, int j) {
-    using RW = Raw<TQ>;
-    const TQ *x = static_cast<const TQ *>(a.q);
-    const TQ *cache = static_cast<const TQ *>(a.cache);
-    const size_t D = (size_t)a.H * DK;
-#pragma unroll
-    for (int i = 0; i < 19; ++i) {
-        const int t = t0 - 3 + i;
-        if (t < 0)  // the cache holds tokens -3, -2, -1 as taps 0, 1, 2
-            raw[i] = RW::load1(cache + ((size_t)m * 9 + 6 + (t + 3)) * D + (size_t)h * DK + j);
-        else if (t < a.T)
-            raw[i] = RW::load1(x + (((size_t)m * a.T + t) * 3 + 2) * D + (size_t)h * DK + j);
-        else
-            raw[i] = RW::zero1();
-    }
-}
-// ... and their conv (kernel 4) + SiLU; tokens past T give 0
-template <typename TQ>
-__device__ __forceinline__ void conv_v(float (&v)[16], const typename Raw<TQ>::V1 (&raw)[19], int t0,
-                                       int T, const float4 w) {
-    using RW = Raw<TQ>;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float pre = w.x * RW::widen1(raw[i]) + w.y * RW::widen1(raw[i + 1]) +
-                          w.z * RW::widen1(raw[i + 2]) + w.w * RW::widen1(raw[i + 3]);
-        v[i] = t0 + i < T ? __fdividef(pre, 1.0f + __expf(-pre)) : 0.f;
-    }
-}
-
 template <typename TQ, bool LAYER, bool NORM>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -281,12 +237,13 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     float *sXch = reinterpret_cast<float *>(sm + S_XCH);
     float *sBeta = reinterpret_cast<float *>(sm + S_BETA);
     float *sGam = reinterpret_cast<float *>(sm + S_GAM);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);  // 0: MMA1, 1: MMA3, 2: MMA4, 3: MMA5/6
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);  // 0: MMA1, 1: MMA3, 2: MMA4, 3: MMA5/6, 4: v
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + S_SLOT);
     float *sA = reinterpret_cast<float *>(sm + T_A);
     float *sT = reinterpret_cast<float *>(sm + T_T);
     float *sX = reinterpret_cast<float *>(sm + T_X);
-    float *sKst = reinterpret_cast<float *>(sm + T_KST);
+    const TQ *sV = reinterpret_cast<const TQ *>(sm + T_V);
+    float *sVc = reinterpret_cast<float *>(sm + S_VC);
     float *sO = reinterpret_cast<float *>(sm + T_O);
     float *sXa = reinterpret_cast<float *>(sm + S_XA);
     float *sXb = reinterpret_cast<float *>(sm + S_XB);
@@ -306,7 +263,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const uint32_t sbase = ptx::smem_u32(sm);
 
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) ptx::mbar_init(&bar[b], 1);
+        for (int b = 0; b < 5; ++b) ptx::mbar_init(&bar[b], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
@@ -343,9 +300,11 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         if (tid < 3 * DK) sWqk[tid] = __ldg(w4 + (size_t)(tid >> 7) * D + (size_t)h * DK + (tid & 127));
         if (tid < DK) sBias[tid] = __ldg(a.dt_bias + (size_t)h * DK + tid);
         const TQ *cache = static_cast<const TQ *>(a.cache);
-        for (int i = tid; i < 2 * 3 * DK; i += NT) {  // xb[1][X][tap][c] = cache[m][X][tap][h, c]
+        for (int i = tid; i < 3 * 3 * DK; i += NT) {  // xb[1][X][tap][c] (q, k) and vc[1][tap][c] (v) = cache
             const int X = i / (3 * DK), tap = (i / DK) % 3, c = i % DK;
-            sXb[XB_F + i] = RW::widen1(RW::load1(cache + ((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c));
+            const float v = RW::widen1(RW::load1(cache + ((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c));
+            if (X < 2) sXb[XB_F + i] = v;
+            else sVc[3 * DK + tap * DK + c] = v;
         }
         if (rh == 0 && rr >= 5) {  // tokens 29-31 of chunk 0 (lanes rr = 5, 6, 7 of g = 3)
             float xq[4], xk[4];
@@ -356,6 +315,20 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         __syncthreads();
     }
+
+    // v of the chunk starting at token t0 -> sV, one bulk copy per token, completing on
+    // bar[4]; called by the 32 lanes of warp kVWarp (lane 0 posts the byte count)
+    auto issue_v = [&](int t0) {
+        const int n = T - t0 < C ? T - t0 : C;
+        const TQ *vsrc = static_cast<const TQ *>(LAYER ? a.q : a.v);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&bar[4], n * DK * (int)sizeof(TQ));
+        for (int t = lane; t < n; t += 32) {
+            const size_t row = LAYER ? (((size_t)m * T + t0 + t) * 3 + 2) * D + (size_t)h * DK
+                                     : (((size_t)m * T + t0 + t) * a.H + h) * DK;
+            ptx::bulk_g2s(const_cast<TQ *>(sV) + t * DK, vsrc + row, DK * sizeof(TQ), &bar[4]);
+        }
+    };
+    if (warp == kVWarp) issue_v(0);
 
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
     const uint32_t id96 = umma::instr_desc(128, 96, umma::kFmtTF32);
@@ -631,22 +604,27 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                      Lk[g][3] * em[3]);
             st_tile4(sm + T_KQ, 64 + r, c4, KB128, Lq[g][0] * em[0], Lq[g][1] * em[1],
                      Lq[g][2] * em[2], Lq[g][3] * em[3]);
-            *reinterpret_cast<float4 *>(sKst + r * LDK + 4 * c4) =
-                make_float4(Rk[g][0] * ed[0], Rk[g][1] * ed[1], Rk[g][2] * ed[2], Rk[g][3] * ed[3]);
+            // Kdec^T tile (row = key channel, K = token): a 4 x 4 transpose among
+            // lanes rr = 4 hh .. 4 hh + 3, after which lane (hh, ce) holds channel
+            // 4 c4 + ce of tokens 8 g + 4 hh .. + 3. Step i: lane sends its element
+            // (ce - i) % 4 and receives token position (ce + i) % 4.
+            const int ce = rr & 3, hh = rr >> 2;
+            const float kc[4] = {Rk[g][0] * ed[0], Rk[g][1] * ed[1], Rk[g][2] * ed[2], Rk[g][3] * ed[3]};
+            float ko[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int es = (ce - i) & 3, pos = (ce + i) & 3;
+                const float send = es == 0 ? kc[0] : (es == 1 ? kc[1] : (es == 2 ? kc[2] : kc[3]));
+                const float recv = __shfl_sync(0xffffffffu, send, 8 * qq + 4 * hh + pos);
+                ko[0] = pos == 0 ? recv : ko[0];
+                ko[1] = pos == 1 ? recv : ko[1];
+                ko[2] = pos == 2 ? recv : ko[2];
+                ko[3] = pos == 3 ? recv : ko[3];
+            }
+            st_tile4(sm + T_KDEC, 4 * c4 + ce, 8 * rh + 2 * g + hh, KB64, ko[0], ko[1], ko[2], ko[3]);
         }
-        __syncthreads();
         // the next chunk's q, k, alpha (the registers of this one are consumed)
         if (c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
-        // Kdec^T tile (row = key channel c, K = token): 16-byte row segments,
-        // 8 consecutive channels per quarter-warp (one core matrix)
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int u = it * NT + tid;
-            const int c8 = u & 7, kq = (u >> 3) & 15, cgr = u >> 7;
-            const int c = 8 * cgr + c8;
-            st_tile4(sm + T_KDEC, c, kq, KB64, sKst[(4 * kq + 0) * LDK + c], sKst[(4 * kq + 1) * LDK + c],
-                     sKst[(4 * kq + 2) * LDK + c], sKst[(4 * kq + 3) * LDK + c]);
-        }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma3, NT);
@@ -663,9 +641,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
         // (runs on CUDA cores while MMA3 is on the tensor cores; v of this
         // chunk is loaded meanwhile)
-        typename RW::V1 vr[LAYER ? 19 : 16];
-        if constexpr (LAYER) load_v19<TQ>(vr, a, m, h, c0 + 16 * hq, j);
-        else load_v<TQ>(vr, a, m, h, c0 + 16 * hq, j);
+
         // 5a. diagonal 16 x 16 blocks, one lane per column: T_bb = (I + A_bb)^-1
         if (warp < 2) {
             const int b = 2 * warp + (lane >> 4), jj = lane & 15, j0 = 16 * b;
@@ -748,13 +724,40 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             break;
         }
         umma::fence_after_sync();
+        if (!ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
+            raise_error(16u);
+            ok = false;
+            break;
+        }
         {
+            // v of tokens 16 hq .. + 15 at channel j from the staged chunk (0 past T)
             float vf[16];
-            if constexpr (LAYER) {
-                conv_v<TQ>(vf, vr, c0 + 16 * hq, T, sWqk[2 * DK + j]);
+            if constexpr (LAYER) {  // conv over tokens 16 hq - 3 .. 16 hq + 15 (the 3 before the chunk kept aside)
+                const float *vc = sVc + ((c0 / C + 1) & 1) * 3 * DK;
+                float raw[19];
+#pragma unroll
+                for (int i = 0; i < 19; ++i) {
+                    const int tl = 16 * hq - 3 + i;  // token within the chunk
+                    raw[i] = tl < 0 ? vc[(tl + 3) * DK + j]
+                                    : (c0 + tl < T ? RW::widen1(reinterpret_cast<const typename RW::V1 *>(sV)[tl * DK + j]) : 0.f);
+                }
+                if (hq == 3) {  // raw v of tokens 61-63, for the next chunk
+                    float *vn = sVc + ((c0 / C) & 1) * 3 * DK;
+#pragma unroll
+                    for (int tap = 0; tap < 3; ++tap) vn[tap * DK + j] = raw[16 + tap];
+                }
+                const float4 wv = sWqk[2 * DK + j];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float pre = wv.x * raw[i] + wv.y * raw[i + 1] + wv.z * raw[i + 2] + wv.w * raw[i + 3];
+                    vf[i] = c0 + 16 * hq + i < T ? __fdividef(pre, 1.0f + __expf(-pre)) : 0.f;
+                }
             } else {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) vf[e] = RW::widen1(vr[e]);
+                for (int e = 0; e < 16; ++e) {
+                    const int tl = 16 * hq + e;
+                    vf[e] = c0 + tl < T ? RW::widen1(reinterpret_cast<const typename RW::V1 *>(sV)[tl * DK + j]) : 0.f;
+                }
             }
             float y[16];  // tokens 16 hq .. 16 hq + 15
             umma::ld_x16(tq + TM_D3 + 16 * hq, y);
@@ -784,6 +787,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
+        if (warp == kVWarp && c0 + C < T) issue_v(c0 + C);
         if (tid == kIssuer) {
 #pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks)
