@@ -93,7 +93,8 @@ constexpr uint32_t T_T = T_A + 64 * LDA * 4;       // T = (I + A)^-1 (plain [64]
 constexpr uint32_t T_X = T_T + 64 * LDA * 4;       // scratch: up to 3 blocks of 16 x 16
 constexpr uint32_t T_V = T_X + 3 * 256 * 4;        // v of the chunk, token-major [64][128] (bulk copies)
 constexpr uint32_t PH2_END = T_V + 64 * DK * 4;
-constexpr uint32_t T_O = 0;                        // O staging [64][128] (phase 7, KQ is dead)
+constexpr uint32_t T_O = T_A;                      // O staging [64][128]: phase 7 to the next chunk's phase 3, over A, T, X
+static_assert(64 * DK * 4 <= T_V - T_A, "O staging fits the A / T / X region");
 static_assert(T_A >= PH1_END, "A and P are written while nothing reads phase-1 tiles");
 constexpr uint32_t TILES = PH2_END > PH1_END ? PH2_END : PH1_END;
 // small buffers (bytes)
@@ -467,8 +468,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
         }
         if (tid < C) sBeta[tid] = beta_n;
-        // the previous chunk's O staging (at the start of the operand tiles) has been read
-        if (warp == 0 && c0 > 0) ptx::bulk_wait_read_all();
         __syncthreads();
         float rq[4], rk[4];
 #pragma unroll
@@ -535,6 +534,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
+        // the previous chunk's O staging (over A, T, X, rewritten from phase 3 on)
+        // has been read by its bulk copies before MMA1 is issued
+        if (warp == 0 && c0 > 0) ptx::bulk_wait_read_all();
         if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma1, NT);
         else ptx::named_bar_arrive(kBarMma1, NT);
         if (tid == kIssuer) {
