@@ -102,8 +102,8 @@ struct Cfg {
     static constexpr int QK_F = DB_F + DK;
     static constexpr int V_F = QK_F + 2 * DK;
     static constexpr int AB_F = V_F + DK;      // [2][DK]: alpha of this head and the next
-    static constexpr int NRM_F = AB_F + 2 * DK;
-    static constexpr int WORK_F = NRM_F + 4;
+    static constexpr int NRM_F = AB_F + 2 * DK;  // [4] norm partials | q.q | q.k | pad
+    static constexpr int WORK_F = NRM_F + 8;
     static constexpr int WORK_BYTES = WORK_F * 4;
     static constexpr int BAR_BYTES = 2 * 8 * 8;        // full[8], issued[8]
     static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
@@ -345,31 +345,57 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         // prefetched at the top of this iteration), visible after barrier 2
         if (GATE && gi >= 0 && un < n_units) gate(ib ^ 1);
 
-        // (c) norms, formed by every warp from shared memory (lane: 4 channels)
-        const float4 q4 = reinterpret_cast<const float4 *>(qkb)[lane];
-        const float4 k4 = reinterpret_cast<const float4 *>(qkb + DK)[lane];
-        float sq = q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w;
-        float sk = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
-        float sqk = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+        // (c) L2 norms. Plain step: they enter only through d and o below, since
+        // u = k_hat.s = rk (k.s), w = rq (q.s) and S' = s + k_hat d = s + k (rk d);
+        // the warps forming d (threads 0-127) take k.k, q.q and q.k and publish
+        // the last two for the warps forming o. With the fused gate and norm
+        // (more live registers in the o warps) every warp forms rq, rk and
+        // k_hat.q_hat itself and the sums below use the normalised q and k.
+        constexpr bool FOLD = !GATE && !NORM;
+        float nA = 0.f;  // k.k in the d warps
+        float rqw = 1.f, rkw = 1.f, kqw = 0.f;
+        if (!FOLD) {
+            const float4 q4 = reinterpret_cast<const float4 *>(qkb)[lane];
+            const float4 k4 = reinterpret_cast<const float4 *>(qkb + DK)[lane];
+            float sq = q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w;
+            float sk = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
+            float sqk = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, off);
-            sk += __shfl_xor_sync(0xffffffffu, sk, off);
-            sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+            for (int off = 16; off > 0; off >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+            }
+            rqw = 1.0f / sqrtf(sq + kL2Eps);
+            rkw = 1.0f / sqrtf(sk + kL2Eps);
+            kqw = sqk * rqw * rkw;
+        } else if (ct < DK) {
+            const float4 q4 = reinterpret_cast<const float4 *>(qkb)[lane];
+            const float4 k4 = reinterpret_cast<const float4 *>(qkb + DK)[lane];
+            nA = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
+            float nQ = q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w;
+            float nB = q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                nA += __shfl_xor_sync(0xffffffffu, nA, off);
+                nQ += __shfl_xor_sync(0xffffffffu, nQ, off);
+                nB += __shfl_xor_sync(0xffffffffu, nB, off);
+            }
+            if (ct == 0) {  // read by the o warps after barrier 3
+                nrm[4] = nQ;
+                nrm[5] = nB;
+            }
         }
-        const float rq = 1.0f / sqrtf(sq + kL2Eps);
-        const float rk = 1.0f / sqrtf(sk + kL2Eps);
-        const float kq = sqk * rq * rk;
 
-        // (d) u = k.s, w = q.s over this thread's rows
+        // (d) column sums k.s and q.s over this thread's rows (raw q, k when folded)
         float uu[C::VEC], ww[C::VEC], kr[C::RPT];
 #pragma unroll
         for (int c = 0; c < C::VEC; ++c) uu[c] = ww[c] = 0.f;
 #pragma unroll
         for (int p = 0; p < C::RPT; ++p) {
             const int row = p * C::RGROUPS + rg;
-            kr[p] = qkb[DK + row] * rk;
-            const float qr = qkb[row] * rq;
+            kr[p] = FOLD ? qkb[DK + row] : qkb[DK + row] * rkw;
+            const float qr = FOLD ? qkb[row] : qkb[row] * rqw;
 #pragma unroll
             for (int c = 0; c < C::VEC; ++c) {
                 uu[c] = fmaf(kr[p], sv[p][c], uu[c]);
@@ -394,20 +420,28 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         }
         ptx::named_bar_sync(bar_id, C::GT);  // barrier 2: partial column sums
 
-        // (e) threads 0-127 form d_j = beta (v_j - u_j); 128-255 sum w_j
+        // (e) threads 0-127 form d_j = beta (v_j - u_j) and publish rk d_j;
+        // 128-255 sum w_j (raw)
         float wt = 0.f;
         if (ct < DK) {
             float ut = 0.f;
 #pragma unroll
             for (int q = 0; q < C::CWARPS; ++q) ut += red[q * DK + ct];
-            db[ct] = beta * (vb[ct] - ut);
+            if (FOLD) {
+                const float rk = 1.0f / sqrtf(nA + kL2Eps);
+                db[ct] = rk * (beta * (vb[ct] - rk * ut));
+            } else {
+                db[ct] = beta * (vb[ct] - ut);
+            }
         } else if (ct < 2 * DK) {
 #pragma unroll
             for (int q = 0; q < C::CWARPS; ++q) wt += redw[q * DK + ct - DK];
         }
         ptx::named_bar_sync(bar_id, C::GT);  // barrier 3: d published
-        if (ct >= DK && ct < 2 * DK) {  // o_j = scale (w_j + d_j (k.q))
-            float oj = a.scale * fmaf(db[ct - DK], kq, wt);
+        if (ct >= DK && ct < 2 * DK) {  // o_j = scale (rq w_j + d_j (k_hat.q_hat)) = scale rq (w_j + (rk d_j) (k.q))
+            float oj;
+            if (FOLD) oj = a.scale * (1.0f / sqrtf(nrm[4] + kL2Eps)) * fmaf(db[ct - DK], nrm[5], wt);
+            else oj = a.scale * fmaf(db[ct - DK], kqw, wt);
             if (NORM) {  // y_j = o_j / sqrt(mean o^2 + eps) * w_j * sigmoid(gate_j)
                 float ss = oj * oj;
 #pragma unroll
