@@ -136,7 +136,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 zero_tx<__nv_bfloat16>() {
 template <typename TX>
 __device__ __forceinline__ float conv_silu(const float4 w, const TX (&win)[3], TX xt) {
     const float pre = w.x * widen(win[0]) + w.y * widen(win[1]) + w.z * widen(win[2]) + w.w * widen(xt);
-    return pre / (1.0f + expf(-pre));
+    return __fdividef(pre, 1.0f + __expf(-pre));
 }
 
 template <typename TS, typename TX, int G>
@@ -207,11 +207,19 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         // back only what it wrote)
         if (has0) wsm[c0] = __ldg(w4 + (size_t)X0 * D + hb + ch0);
         if (has1) wsm[c1] = __ldg(w4 + (size_t)X1 * D + hb + ch1);
-        // inputs of token 0 (loaded while the stage lands) and of token 1
-        TX xn0 = has0 ? xp0[0] : zero_tx<TX>();
-        TX xn1 = has1 ? xp0[off1] : zero_tx<TX>();
-        float an = ct < DK ? __ldg(ap) : 0.f;
+        // inputs of tokens 0 and 1, loaded while the stage lands
+        const TX x00 = has0 ? xp0[0] : zero_tx<TX>();
+        const TX x10 = has1 ? xp0[off1] : zero_tx<TX>();
+        const float a0 = ct < DK ? __ldg(ap) : 0.f;
         float beta_c = __ldg(bp), beta_n = 0.f;
+        TX xn0 = zero_tx<TX>(), xn1 = zero_tx<TX>();
+        float an = 0.f;
+        if (T > 1) {
+            if (has0) xn0 = xp0[xs];
+            if (has1) xn1 = xp0[xs + off1];
+            if (ct < DK) an = __ldg(ap + as);
+            beta_n = __ldg(bp + H);
+        }
 
         if ((n > 0 && !ptx::mbar_wait(&issued[s], (n - 1) & 1, kWaitBudget)) ||
             !ptx::mbar_wait(&full[s], n & 1, kWaitBudget)) {
@@ -234,32 +242,26 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             if (has1) win[j * 3 * DK + c1] = cs[(X1 * 3 + j) * DK + ch1];
         }
         // convolve the buffered inputs of one token into a token buffer
-        auto convolve = [&](float *b, float al) {
+        auto convolve = [&](float *b, float al, TX xa, TX xb) {
             if (has0) {
                 const TX w0 = win[c0], w1 = win[3 * DK + c0], w2 = win[6 * DK + c0];
                 const TX wv[3] = {w0, w1, w2};
-                b[dst0] = conv_silu(wsm[c0], wv, xn0);
+                b[dst0] = conv_silu(wsm[c0], wv, xa);
                 win[c0] = w1;
                 win[3 * DK + c0] = w2;
-                win[6 * DK + c0] = xn0;
+                win[6 * DK + c0] = xa;
             }
             if (has1) {
                 const TX w0 = win[c1], w1 = win[3 * DK + c1], w2 = win[6 * DK + c1];
                 const TX wv[3] = {w0, w1, w2};
-                b[dst1] = conv_silu(wsm[c1], wv, xn1);
+                b[dst1] = conv_silu(wsm[c1], wv, xb);
                 win[c1] = w1;
                 win[3 * DK + c1] = w2;
-                win[6 * DK + c1] = xn1;
+                win[6 * DK + c1] = xb;
             }
             if (ct < DK) b[2 * DK + perm_row(ct)] = al;
         };
-        convolve(buf, an);
-        if (T > 1) {
-            if (has0) xn0 = xp0[xs];
-            if (has1) xn1 = xp0[xs + off1];
-            if (ct < DK) an = __ldg(ap + as);
-            beta_n = __ldg(bp + H);
-        }
+        convolve(buf, a0, x00, x10);
         ptx::named_bar_sync(bar_id, C::GT);  // stage read; token 0 in buffer 0
         if (ct == 0) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
@@ -273,7 +275,7 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             const float *bc = buf + (t & 1) * C::BUF_F;
             const float beta = beta_c;
             if (t + 1 < T) {  // convolve token t + 1 into the other buffer, load token t + 2
-                convolve(buf + ((t + 1) & 1) * C::BUF_F, an);
+                convolve(buf + ((t + 1) & 1) * C::BUF_F, an, xn0, xn1);
                 beta_c = beta_n;
                 if (t + 2 < T) {
                     if (has0) xn0 = xp0[(size_t)(t + 2) * xs];
