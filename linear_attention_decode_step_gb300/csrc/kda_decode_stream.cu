@@ -45,9 +45,11 @@
 //    y = o / sqrt(mean o^2 + eps) w sigmoid(gate)), applied by the 128 threads
 //    that form o, with one 128-thread barrier for the sum of squares.
 //  * Launched with programmatic stream serialisation: the kernel waits for
-//    the preceding grid (griddepcontrol.wait) before its first global access,
+//    the preceding grid (griddepcontrol.wait) before its first global read,
 //    and lets the next launch in the stream start placing CTAs early, which
-//    hides launch latency between back-to-back layers.
+//    hides launch latency between back-to-back layers. Before the wait it
+//    only prefetches its first heads' state into L2 (a hint; L2 also holds
+//    whatever the previous grid writes).
 //
 // Each conv-cache channel belongs to exactly one head, so the cache is read
 // (by the bulk copy) and rewritten (by the consumer) by one CTA only.
@@ -215,6 +217,16 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             ptx::mbar_init(&issued[s], 1);
         }
         ptx::fence_mbar_init();
+    }
+    // While the previous grid drains, warm L2 with the state of this CTA's
+    // first heads. A prefetch only fills L2, where the previous grid's writes
+    // land as well, so it cannot expose stale data; the copies below (after
+    // the dependency wait) then hit L2 instead of paying DRAM latency.
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units) prefetch_head<TS>(a, u);
+        }
     }
     __syncthreads();
     ptx::grid_dependency_wait();  // the previous grid's writes are visible from here on

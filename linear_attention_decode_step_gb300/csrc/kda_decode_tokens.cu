@@ -160,6 +160,15 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         }
         ptx::fence_mbar_init();
     }
+    // warm L2 with the first heads' state while the previous grid drains (a
+    // hint only: L2 also receives whatever the previous grid writes)
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units)
+                ptx::bulk_prefetch_l2(static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES);
+        }
+    }
     __syncthreads();
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
