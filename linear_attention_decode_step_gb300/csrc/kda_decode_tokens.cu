@@ -241,9 +241,17 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         const TX *cs = reinterpret_cast<const TX *>(st + C::C_OFF);
 
         float *op = a.o + ((size_t)m * T * H + h) * DK + ocol;
-        float sv[16][4];
+        // the state as column pairs: the FP32 arithmetic below runs on packed
+        // pairs (fma.rn.f32x2 / mul.rn.f32x2: two exactly rounded FP32
+        // operations per instruction)
+        float2 sv[16][2];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Quad<TS>::load(Ss + (rl + 8 * r) * DK + col0, sv[r]);
+        for (int r = 0; r < 16; ++r) {
+            float f4[4];
+            Quad<TS>::load(Ss + (rl + 8 * r) * DK + col0, f4);
+            sv[r][0] = make_float2(f4[0], f4[1]);
+            sv[r][1] = make_float2(f4[2], f4[3]);
+        }
         // conv windows (oldest first, exactly as stored); each thread owns its channels' slots
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
@@ -314,7 +322,8 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             const float rk = rsqrtf(sk + kL2Eps);
 
             // fade, then raw column sums over this lane's 16 rows
-            float uu[4] = {0.f, 0.f, 0.f, 0.f}, ww[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 uu2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 ww2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int r4 = 0; r4 < 4; ++r4) {
                 const float4 q4 = *reinterpret_cast<const float4 *>(qb + 4 * r4);
@@ -325,14 +334,19 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int r = 4 * r4 + e;
+                    const float2 a2 = make_float2(av[e], av[e]);
+                    const float2 k2 = make_float2(kv[e], kv[e]);
+                    const float2 q2 = make_float2(qv[e], qv[e]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        sv[r][c] *= av[e];
-                        uu[c] = fmaf(kv[e], sv[r][c], uu[c]);
-                        ww[c] = fmaf(qv[e], sv[r][c], ww[c]);
+                    for (int c = 0; c < 2; ++c) {
+                        sv[r][c] = __fmul2_rn(sv[r][c], a2);
+                        uu2[c] = __ffma2_rn(k2, sv[r][c], uu2[c]);
+                        ww2[c] = __ffma2_rn(q2, sv[r][c], ww2[c]);
                     }
                 }
             }
+            const float uu[4] = {uu2[0].x, uu2[0].y, uu2[1].x, uu2[1].y};
+            const float ww[4] = {ww2[0].x, ww2[0].y, ww2[1].x, ww2[1].y};
             // reduce over the 8 lane groups rl, halving the values at each level
             const bool b2 = lane & 16, b1 = lane & 8, b0 = lane & 4;
             float x4[4];
@@ -358,14 +372,17 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             float dd[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) dd[e] = __shfl_sync(0xffffffffu, dk, 4 * e + cc);
+            const float2 dd2[2] = {make_float2(dd[0], dd[1]), make_float2(dd[2], dd[3])};
 #pragma unroll
             for (int r4 = 0; r4 < 4; ++r4) {
                 const float4 k4 = *reinterpret_cast<const float4 *>(kb + 4 * r4);
                 const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
+                for (int e = 0; e < 4; ++e) {
+                    const float2 k2 = make_float2(kv[e], kv[e]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) sv[4 * r4 + e][c] = fmaf(kv[e], dd[c], sv[4 * r4 + e][c]);
+                    for (int c = 0; c < 2; ++c) sv[4 * r4 + e][c] = __ffma2_rn(k2, dd2[c], sv[4 * r4 + e][c]);
+                }
             }
             ptx::named_bar_sync(bar_id, C::GT);  // token t + 1 convolved; buffer t free
         }
@@ -373,7 +390,10 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         // state out (rounded once, here, for BF16 storage) and the final conv windows
         TS *Sg = static_cast<TS *>(a.state) + (size_t)u * DK * DK + col0;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Quad<TS>::store(Sg + (size_t)(rl + 8 * r) * DK, sv[r]);
+        for (int r = 0; r < 16; ++r) {
+            const float f4[4] = {sv[r][0].x, sv[r][0].y, sv[r][1].x, sv[r][1].y};
+            Quad<TS>::store(Sg + (size_t)(rl + 8 * r) * DK, f4);
+        }
         const size_t cbase = (size_t)m * 9 * D + hb;
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
