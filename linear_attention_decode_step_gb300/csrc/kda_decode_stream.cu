@@ -324,8 +324,13 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             const uint4 r = *reinterpret_cast<const uint4 *>(Ss + row * DK + strip * C::VEC);
             Strip<TS>::unpack(r, sv[p]);
             const float ar = GATE ? ab[ib * DK + row] : al[row];
+            const float2 a2 = make_float2(ar, ar);
 #pragma unroll
-            for (int c = 0; c < C::VEC; ++c) sv[p][c] *= ar;
+            for (int c = 0; c < C::VEC; c += 2) {  // packed FP32 pairs (mul.rn.f32x2)
+                const float2 f = __fmul2_rn(make_float2(sv[p][c], sv[p][c + 1]), a2);
+                sv[p][c] = f.x;
+                sv[p][c + 1] = f.y;
+            }
         }
 
         // (b) conv + SiLU of the head's 384 channels (q, k, v)
@@ -408,10 +413,16 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             const int row = p * C::RGROUPS + rg;
             kr[p] = FOLD ? qkb[DK + row] : qkb[DK + row] * rkw;
             const float qr = FOLD ? qkb[row] : qkb[row] * rqw;
+            const float2 k2 = make_float2(kr[p], kr[p]), q2 = make_float2(qr, qr);
 #pragma unroll
-            for (int c = 0; c < C::VEC; ++c) {
-                uu[c] = fmaf(kr[p], sv[p][c], uu[c]);
-                ww[c] = fmaf(qr, sv[p][c], ww[c]);
+            for (int c = 0; c < C::VEC; c += 2) {  // packed FP32 pairs (fma.rn.f32x2)
+                const float2 s2 = make_float2(sv[p][c], sv[p][c + 1]);
+                const float2 u2 = __ffma2_rn(k2, s2, make_float2(uu[c], uu[c + 1]));
+                const float2 w2 = __ffma2_rn(q2, s2, make_float2(ww[c], ww[c + 1]));
+                uu[c] = u2.x;
+                uu[c + 1] = u2.y;
+                ww[c] = w2.x;
+                ww[c + 1] = w2.y;
             }
         }
         if (C::SUBS == 2) {
@@ -481,8 +492,14 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         for (int p = 0; p < C::RPT; ++p) {
             const int row = p * C::RGROUPS + rg;
             float nv[C::VEC];
+            const float2 k2 = make_float2(kr[p], kr[p]);
 #pragma unroll
-            for (int c = 0; c < C::VEC; ++c) nv[c] = fmaf(kr[p], dd[c], sv[p][c]);
+            for (int c = 0; c < C::VEC; c += 2) {  // packed FP32 pairs (fma.rn.f32x2)
+                const float2 n2 = __ffma2_rn(k2, make_float2(dd[c], dd[c + 1]),
+                                             make_float2(sv[p][c], sv[p][c + 1]));
+                nv[c] = n2.x;
+                nv[c + 1] = n2.y;
+            }
             __stcs(reinterpret_cast<uint4 *>(Sg + (size_t)row * DK), Strip<TS>::pack(nv));
         }
     }
