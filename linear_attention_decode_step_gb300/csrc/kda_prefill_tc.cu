@@ -40,18 +40,19 @@
 // (qq, rr) = (lane / 8, lane % 8) holds tokens 8 g + rr (g = 0..3) of the half
 // and channels 4 qq .. + 3 of the warp's group. A quarter-warp (8 lanes, the
 // unit in which 16-byte shared-memory stores are served) thus writes the 8
-// rows of one core matrix: the tile stores are free of bank conflicts. "Tensor-memory" work: warp w
-// reads lanes 32 (w % 4) .. + 31 (value channel j) and column quarter w / 4.
+// rows of one core matrix: the tile stores are free of bank conflicts.
+// "Tensor-memory" work: warp w reads lanes 32 (w % 4) .. + 31 (value channel
+// j) and column quarter w / 4.
 //
 // The unit lower-triangular inverse is taken on CUDA cores in 16 x 16 blocks:
 // diagonal blocks by forward substitution (one lane per column), off-diagonal
 // blocks level by level from the block recurrence T_RI = -T_RR sum_Q A_RQ T_QI.
 //
-// Inputs are loaded into registers ahead of use: q, k, alpha of the next
-// chunk once this chunk's operand tiles are built, v of this chunk while the
-// inverse is formed. O leaves through shared memory with bulk copies. Every mbarrier
-// wait is bounded; on timeout the kernel sets the device error word
-// (kda_device_error) and stops.
+// Inputs arrive ahead of use: q, k, alpha of the next chunk are loaded into
+// registers once this chunk's operand tiles are built; v of the next chunk is
+// brought into shared memory by bulk copies from a side warp. O leaves through
+// shared memory with bulk copies. Every mbarrier wait is bounded; on timeout
+// the kernel sets the device error word (kda_device_error) and stops.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
