@@ -626,8 +626,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
             st_tile4(sm + T_KDEC, 4 * c4 + ce, 8 * rh + 2 * g + hh, KB64, ko[0], ko[1], ko[2], ko[3]);
         }
-        // the next chunk's q, k, alpha (the registers of this one are consumed)
-        if (c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
         umma::fence_smem_to_async();
         umma::fence_before_sync();
         if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma3, NT);
@@ -640,6 +638,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                              umma::smem_desc(sbase + T_KQ + ks * 256, 128, 8 * KB128), id128, ks > 0);
             umma::commit(&bar[1]);
         }
+        // the next chunk's q, k, alpha (the registers of this one are consumed);
+        // issued after the proxy fence above, which would otherwise wait for them
+        if (c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
 
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
         // (runs on CUDA cores while MMA3 is on the tensor cores; v of this
