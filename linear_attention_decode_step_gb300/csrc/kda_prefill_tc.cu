@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const uint32_t id96 = umma::instr_desc(128, 96, umma::kFmtTF32);
     const uint32_t id64 = umma::instr_desc(128, 64, umma::kFmtTF32);
     bool ok = true;
+    int v_pending = 1;  // a bulk copy of v is in flight (completion parity: v_parity)
+    int v_parity = 0;
     int phase = 0;
 
     for (int c0 = 0; c0 < T && ok; c0 += C, phase ^= 1) {
@@ -728,7 +730,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             break;
         }
         umma::fence_after_sync();
-        if (!ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
+        if (ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
+            v_pending = 0;
+        } else {
             raise_error(16u);
             ok = false;
             break;
@@ -792,6 +796,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         __syncthreads();
         umma::fence_after_sync();
         if (warp == kVWarp && c0 + C < T) issue_v(c0 + C);
+        if (c0 + C < T) {
+            v_pending = 1;
+            v_parity = phase ^ 1;
+        }
         if (tid == kIssuer) {
 #pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks)
@@ -865,6 +873,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             ptx::bulk_commit();
         }
     }
+
+    // after a timeout, let a bulk copy still in flight land before the CTA's
+    // shared memory goes (bounded as well)
+    if (!ok && v_pending) ptx::mbar_wait(&bar[4], v_parity, kWaitBudget);
 
     // state out
     if (ok) {
