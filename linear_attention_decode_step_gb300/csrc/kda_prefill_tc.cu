@@ -480,8 +480,18 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             const float4 qb = *reinterpret_cast<const float4 *>(sNorm + r * LDN + 4);
             const float4 ka = *reinterpret_cast<const float4 *>(sNorm + (64 + r) * LDN);
             const float4 kb = *reinterpret_cast<const float4 *>(sNorm + (64 + r) * LDN + 4);
-            rq[g] = 1.0f / sqrtf(qa.x + qa.y + qa.z + qa.w + qb.x + qb.y + qb.z + qb.w + kL2Eps);
-            rk[g] = 1.0f / sqrtf(ka.x + ka.y + ka.z + ka.w + kb.x + kb.y + kb.z + kb.w + kL2Eps);
+            const float sq = qa.x + qa.y + qa.z + qa.w + qb.x + qb.y + qb.z + qb.w + kL2Eps;
+            const float sk = ka.x + ka.y + ka.z + ka.w + kb.x + kb.y + kb.z + kb.w + kL2Eps;
+            // The layer form takes the hardware reciprocal square root (a few
+            // ulp, far inside the TF32 operand error); the plain form keeps
+            // the correctly rounded one, which schedules without spills there.
+            if constexpr (LAYER) {
+                rq[g] = rsqrtf(sq);
+                rk[g] = rsqrtf(sk);
+            } else {
+                rq[g] = 1.0f / sqrtf(sq);
+                rk[g] = 1.0f / sqrtf(sk);
+            }
         }
         // per-channel factors (log2 units):
         //   half 0: u = e^{G - G_15};  R0o = K e^{m_1 - G} with m_1 = G_31 + L_47
