@@ -54,10 +54,12 @@
 // shared memory with bulk copies. Every mbarrier wait is bounded; on timeout
 // the kernel sets the device error word (kda_device_error) and stops.
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
@@ -117,12 +119,23 @@ constexpr uint32_t S_BAR = S_VC + 2 * 3 * 128 * 4; // 5 mbarriers
 constexpr uint32_t S_SLOT = S_BAR + 6 * 8;
 constexpr uint32_t SMEM_BYTES = S_SLOT + 16;
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KiB opt-in shared memory");
+// BF16 q, k: q, k and alpha of the next chunk are staged in the [Kd; Qd]
+// region (free from the completion of MMA3 to the next chunk's operand
+// stores) as tensor-copy boxes of 64 tokens x 128 bytes, 128-byte swizzled
+constexpr uint32_t BOX = 64 * 128;
+constexpr uint32_t ST_Q = T_KQ;                    // 2 boxes of 64 channels (BF16)
+constexpr uint32_t ST_K = ST_Q + 2 * BOX;          // 2 boxes
+constexpr uint32_t ST_AL = ST_K + 2 * BOX;         // 4 boxes of 32 channels (FP32)
+constexpr uint32_t ST_END = ST_AL + 4 * BOX;
+static_assert(ST_END <= T_KDEC, "the staging fits the [Kd; Qd] region");
+static_assert(T_V % 1024 == 0 && T_O % 1024 == 0, "tensor-copy boxes start 1024-byte aligned");
 
 // the thread that issues every MMA: lane 0 of the last warp (free of the
 // phase-specific work that warps 0-1 carry in the inverse)
 constexpr int kIssuer = NT - 32;
-// the warp that issues the bulk copies of v
+// lane 0 of this warp issues the tensor copies of q, k, alpha and v
 constexpr int kVWarp = NT / 32 - 2;
+constexpr int kLoader = 32 * kVWarp;
 // named barriers (0 is __syncthreads): the issuer waits for all threads,
 // the others only signal and move on
 constexpr uint32_t kBarMma1 = 1, kBarMma3 = 2, kBarOut = 3;
@@ -132,6 +145,24 @@ constexpr uint32_t TM_S = 0, TM_D3 = 128, TM_Z = 256, TM_D4 = 320, TM_D1 = 384;
 constexpr uint32_t TM_COLS = 512;
 
 __device__ __forceinline__ void raise_error(unsigned int code) { atomicOr(&g_prefill_error, code); }
+
+// Tensor maps of one call (made on the host, kernel parameter). Every map
+// views its tensor with the channel innermost, then head, [tensor,] token,
+// stream, so that a box is 64 tokens of one head and tokens past T read as 0.
+struct PrefillMaps {
+    CUtensorMap q;      // q [M][T][H][128]; the layer form: x [M][T][3][H*128] (q and k); 128-byte swizzle
+    CUtensorMap k;      // k (plain form); 128-byte swizzle
+    CUtensorMap alpha;  // alpha, or the raw gate input of the layer form; 128-byte swizzle
+    CUtensorMap v;      // v, or x of the layer form (tensor 2); boxes of 64 x 128 channels
+    CUtensorMap o;      // o [M][T][H][128]; boxes of 64 x 128 channels (stores)
+};
+
+// Byte offset of (row, byte) in a box of 128-byte rows written with the
+// 128-byte swizzle: the 16-byte chunk index is XORed with the row index
+// modulo 8 (the box starts 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t byte) {
+    return row * 128u + ((((byte >> 4) ^ row) & 7u) << 4) + (byte & 15u);
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -232,14 +263,37 @@ __device__ __forceinline__ void load_qka(QKA<TQ> &R, const PrefillArgs &a, int m
         }
     }
 }
+// The same values from the staged boxes (BF16 q, k): channels 4 c4 .. + 3
+// sit in q / k box c4 / 16 at byte 8 (c4 % 16) and in alpha box c4 / 8 at
+// byte 16 (c4 % 8). Lanes rr = 0..7 read rows of distinct residues mod 8, so
+// the swizzle spreads a quarter-warp over all 32 banks.
+__device__ __forceinline__ void fetch_qka(QKA<__nv_bfloat16> &R, const unsigned char *sm, int r0, int c4) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t r = r0 + 8 * g;
+        R.q[g] = *reinterpret_cast<const uint2 *>(sm + ST_Q + (c4 >> 4) * BOX + swz(r, (c4 & 15) * 8));
+        R.k[g] = *reinterpret_cast<const uint2 *>(sm + ST_K + (c4 >> 4) * BOX + swz(r, (c4 & 15) * 8));
+        R.al[g] = *reinterpret_cast<const float4 *>(sm + ST_AL + (c4 >> 3) * BOX + swz(r, (c4 & 7) * 16));
+    }
+}
+// One staged raw BF16 value: tensor X (0 q, 1 k), token row, channel c.
+__device__ __forceinline__ float staged1(const unsigned char *sm, int X, int row, int c) {
+    const unsigned short u =
+        *reinterpret_cast<const unsigned short *>(sm + (X ? ST_K : ST_Q) + (c >> 6) * BOX + swz(row, (c & 63) * 2));
+    return __uint_as_float((uint32_t)u << 16);
+}
+
 template <typename TQ, bool LAYER, bool NORM>
-__global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ PrefillMaps mp) {
+    // BF16 q, k arrive by tensor copies into shared memory; FP32 ones (twice
+    // the bytes: no room to stage) by register loads a chunk ahead
+    constexpr bool kTma = sizeof(TQ) == 2;
     extern __shared__ __align__(1024) unsigned char sm[];
     float *sNorm = reinterpret_cast<float *>(sm + S_NORM);
     float *sXch = reinterpret_cast<float *>(sm + S_XCH);
     float *sBeta = reinterpret_cast<float *>(sm + S_BETA);
     float *sGam = reinterpret_cast<float *>(sm + S_GAM);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);  // 0: MMA1, 1: MMA3, 2: MMA4, 3: MMA5/6, 4: v
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);  // 0: MMA1, 1: MMA3, 2: MMA4, 3: MMA5/6, 4: v, 5: q, k, alpha
     uint32_t *slot = reinterpret_cast<uint32_t *>(sm + S_SLOT);
     float *sA = reinterpret_cast<float *>(sm + T_A);
     float *sT = reinterpret_cast<float *>(sm + T_T);
@@ -263,9 +317,13 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const int j = 32 * q4 + lane;                  // value channel (TMEM lane)
     const int T = a.T;
     const uint32_t sbase = ptx::smem_u32(sm);
+    if (sbase & 1023u) {  // the swizzled boxes need a 1024-byte aligned base
+        if (tid == 0) raise_error(64u);
+        return;
+    }
 
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) ptx::mbar_init(&bar[b], 1);
+        for (int b = 0; b < 6; ++b) ptx::mbar_init(&bar[b], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
@@ -291,7 +349,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     using RW = Raw<TQ>;
     QKA<TQ> R;
     float beta_n = 0.f;
-    load_qka<TQ, LAYER>(R, a, m, h, r0, c4);
+    if (!kTma) load_qka<TQ, LAYER>(R, a, m, h, r0, c4);
     if (tid < C) beta_n = tid < T ? __ldg(a.beta + ((size_t)m * T + tid) * a.H + h) : 0.f;
 
     // the layer form: gate constants, conv weights, the cache as the tokens
@@ -308,7 +366,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             if (X < 2) sXb[XB_F + i] = v;
             else sVc[3 * DK + tap * DK + c] = v;
         }
-        if (rh == 0 && rr >= 5) {  // tokens 29-31 of chunk 0 (lanes rr = 5, 6, 7 of g = 3)
+        if (!kTma && rh == 0 && rr >= 5) {  // tokens 29-31 of chunk 0 (lanes rr = 5, 6, 7 of g = 3)
             float xq[4], xk[4];
             RW::widen4(R.q[3], xq);
             RW::widen4(R.k[3], xk);
@@ -318,30 +376,55 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         __syncthreads();
     }
 
-    // v of the chunk starting at token t0 -> sV, one bulk copy per token, completing on
-    // bar[4]; called by the 32 lanes of warp kVWarp (lane 0 posts the byte count)
+    // v of the chunk starting at token t0 -> sV (token-major [64][128], rows
+    // past T zero), one tensor copy completing on bar[4]; thread kLoader
     auto issue_v = [&](int t0) {
-        const int n = T - t0 < C ? T - t0 : C;
-        const TQ *vsrc = static_cast<const TQ *>(LAYER ? a.q : a.v);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&bar[4], n * DK * (int)sizeof(TQ));
-        for (int t = lane; t < n; t += 32) {
-            const size_t row = LAYER ? (((size_t)m * T + t0 + t) * 3 + 2) * D + (size_t)h * DK
-                                     : (((size_t)m * T + t0 + t) * a.H + h) * DK;
-            ptx::bulk_g2s(const_cast<TQ *>(sV) + t * DK, vsrc + row, DK * sizeof(TQ), &bar[4]);
-        }
+        ptx::mbar_arrive_expect_tx(&bar[4], C * DK * (uint32_t)sizeof(TQ));
+        if (LAYER) ptx::tma_load_5d(sm + T_V, &mp.v, &bar[4], 0, h, 2, t0, m);
+        else ptx::tma_load_4d(sm + T_V, &mp.v, &bar[4], 0, h, t0, m);
     };
-    if (warp == kVWarp) issue_v(0);
+    // BF16 q, k: q, k, alpha of the chunk at t0 -> the staging boxes, completing on bar[5]
+    auto issue_qka = [&](int t0) {
+        ptx::mbar_arrive_expect_tx(&bar[5], ST_END - ST_Q);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            if (LAYER) {
+                ptx::tma_load_5d(sm + ST_Q + b * BOX, &mp.q, &bar[5], 64 * b, h, 0, t0, m);
+                ptx::tma_load_5d(sm + ST_K + b * BOX, &mp.q, &bar[5], 64 * b, h, 1, t0, m);
+            } else {
+                ptx::tma_load_4d(sm + ST_Q + b * BOX, &mp.q, &bar[5], 64 * b, h, t0, m);
+                ptx::tma_load_4d(sm + ST_K + b * BOX, &mp.k, &bar[5], 64 * b, h, t0, m);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) ptx::tma_load_4d(sm + ST_AL + b * BOX, &mp.alpha, &bar[5], 32 * b, h, t0, m);
+    };
+    if (tid == kLoader) {
+        if (kTma) issue_qka(0);
+        issue_v(0);
+    }
 
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
     const uint32_t id96 = umma::instr_desc(128, 96, umma::kFmtTF32);
     const uint32_t id64 = umma::instr_desc(128, 64, umma::kFmtTF32);
     bool ok = true;
-    int v_pending = 1;  // a bulk copy of v is in flight (completion parity: v_parity)
+    int v_pending = 1;  // a tensor copy of v is in flight (completion parity: v_parity)
     int v_parity = 0;
+    int qka_pending = kTma;  // the same for the staged q, k, alpha
+    int qka_parity = 0;
     int phase = 0;
 
     for (int c0 = 0; c0 < T && ok; c0 += C, phase ^= 1) {
         // ---------------------------------------------------------- 1. decay, norms
+        if constexpr (kTma) {
+            if (!ptx::mbar_wait(&bar[5], phase, kWaitBudget)) {
+                raise_error(32u);
+                ok = false;
+                break;
+            }
+            qka_pending = 0;
+            fetch_qka(R, sm, r0, c4);
+        }
         // cumulative log2-decay over the half's 32 tokens (lanes rr, then g)
         float G[4][4], qf[4][4], kf[4][4];
 #pragma unroll
@@ -395,6 +478,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                         if (g > 0) {
                             bq = __shfl_sync(0xffffffffu, qf[g > 0 ? g - 1 : 0][e], src);
                             bk = __shfl_sync(0xffffffffu, kf[g > 0 ? g - 1 : 0][e], src);
+                        } else if (kTma && rh == 1) {  // tokens 29-31 from the staged boxes
+                            const int tap = rr - kk + 3 < 2 ? rr - kk + 3 : 2;  // used only when rr < kk
+                            bq = staged1(sm, 0, 29 + tap, 4 * c4 + e);
+                            bk = staged1(sm, 1, 29 + tap, 4 * c4 + e);
                         } else {
                             const int tap = rr - kk + 3 < 2 ? rr - kk + 3 : 2;  // used only when rr < kk
                             bq = xp[(0 * 3 + tap) * DK + 4 * c4 + e];
@@ -413,11 +500,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
         } else {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                G[g][0] = lg2(R.al[g].x);
-                G[g][1] = lg2(R.al[g].y);
-                G[g][2] = lg2(R.al[g].z);
-                G[g][3] = lg2(R.al[g].w);
+            for (int g = 0; g < 4; ++g) {  // tokens past T: no decay (staged alpha reads 0 there)
+                const bool live = c0 + 32 * rh + 8 * g + rr < T;
+                G[g][0] = live ? lg2(R.al[g].x) : 0.f;
+                G[g][1] = live ? lg2(R.al[g].y) : 0.f;
+                G[g][2] = live ? lg2(R.al[g].z) : 0.f;
+                G[g][3] = live ? lg2(R.al[g].w) : 0.f;
             }
         }
         float carry[4] = {0.f, 0.f, 0.f, 0.f};
@@ -549,7 +637,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_before_sync();
         // the previous chunk's O staging (over A, T, X, rewritten from phase 3 on)
         // has been read by its bulk copies before MMA1 is issued
-        if (warp == 0 && c0 > 0) ptx::bulk_wait_read_all();
+        if (tid == 0 && c0 > 0) ptx::bulk_wait_read_all();
         if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma1, NT);
         else ptx::named_bar_arrive(kBarMma1, NT);
         if (tid == kIssuer) {
@@ -652,7 +740,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         // the next chunk's q, k, alpha (the registers of this one are consumed);
         // issued after the proxy fence above, which would otherwise wait for them
-        if (c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
+        if (!kTma && c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
 
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
         // (runs on CUDA cores while MMA3 is on the tensor cores; v of this
@@ -740,6 +828,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             break;
         }
         umma::fence_after_sync();
+        // MMA3 has read [Kd; Qd]: the region takes the next chunk's q, k, alpha
+        if (kTma && c0 + C < T) {
+            if (tid == kLoader) issue_qka(c0 + C);
+            qka_pending = 1;
+            qka_parity = phase ^ 1;
+        }
         if (ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
             v_pending = 0;
         } else {
@@ -794,7 +888,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         umma::wait_st();
         // the layer form: raw q, k of tokens 29-31 of the next chunk (loaded in phase 4)
-        if (LAYER && rh == 0 && rr >= 5 && c0 + C < T) {
+        if (!kTma && LAYER && rh == 0 && rr >= 5 && c0 + C < T) {
             float xq[4], xk[4];
             RW::widen4(R.q[3], xq);
             RW::widen4(R.k[3], xk);
@@ -805,7 +899,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
-        if (warp == kVWarp && c0 + C < T) issue_v(c0 + C);
+        if (tid == kLoader && c0 + C < T) issue_v(c0 + C);
         if (c0 + C < T) {
             v_pending = 1;
             v_parity = phase ^ 1;
@@ -872,14 +966,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_before_sync();
         if (warp == 0) ptx::named_bar_sync(kBarOut, NT);
         else ptx::named_bar_arrive(kBarOut, NT);
-        if (warp == 0) {
-            const int nt = T - c0 < C ? T - c0 : C;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = lane + 32 * e;
-                if (t < nt)
-                    ptx::bulk_s2g(a.o + (((size_t)m * T + c0 + t) * a.H + h) * DK, sO + t * DK, DK * 4);
-            }
+        if (tid == 0) {  // rows past T fall outside the tensor and are not written
+            ptx::tma_store_4d(&mp.o, sO, 0, h, c0, m);
             ptx::bulk_commit();
         }
     }
@@ -887,6 +975,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     // after a timeout, let a bulk copy still in flight land before the CTA's
     // shared memory goes (bounded as well)
     if (!ok && v_pending) ptx::mbar_wait(&bar[4], v_parity, kWaitBudget);
+    if (!ok && qka_pending) ptx::mbar_wait(&bar[5], qka_parity, kWaitBudget);
 
     // state out
     if (ok) {
@@ -913,18 +1002,91 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         for (int tap = 0; tap < 3; ++tap)
             reinterpret_cast<typename RW::V1 *>(cache)[((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c] = nv[tap];
     }
-    if (warp == 0) ptx::bulk_wait_all();  // O copies complete before the CTA's shared memory goes
+    if (tid == 0) ptx::bulk_wait_all();  // O stores complete before the CTA's shared memory goes
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tb, TM_COLS);
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link
+// against the driver library)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A map over a row-major tensor whose dims are listed innermost first
+// (dims[0] = 128 channels, contiguous); strides follow from the dims, box
+// dims as given, zero fill outside the tensor.
+cudaError_t make_map(CUtensorMap *map, const void *base, bool bf16, int rank, const uint64_t *dims,
+                     const uint32_t *box, bool swizzle) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const uint64_t esz = bf16 ? 2 : 4;
+    cuuint64_t gdim[5], gstr[4];
+    cuuint32_t bdim[5], estr[5];
+    uint64_t stride = esz;
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) gstr[i - 1] = stride;
+        stride *= dims[i];
+    }
+    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          (cuuint32_t)rank, const_cast<void *>(base), gdim, gstr, bdim, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename TQ, bool LAYER>
+cudaError_t make_maps(const PrefillArgs &a, PrefillMaps *mp) {
+    const bool bf16 = sizeof(TQ) == 2;
+    const uint64_t H = a.H, T = a.T, M = a.M;
+    const uint64_t d4[4] = {DK, H, T, M};   // [M][T][H][128]
+    const uint64_t d5[5] = {DK, H, 3, T, M};  // [M][T][3][H*128]
+    const uint32_t box_half[5] = {64, 1, 1, C, 1};  // 128 bytes of BF16 channels (swizzled)
+    const uint32_t box_al[4] = {32, 1, C, 1};      // 128 bytes of FP32 channels (swizzled)
+    const uint32_t box_row4[4] = {DK, 1, C, 1};
+    const uint32_t box_row5[5] = {DK, 1, 1, C, 1};
+    const uint32_t box_half4[4] = {64, 1, C, 1};
+    cudaError_t e = cudaSuccess;
+    memset(mp, 0, sizeof(PrefillMaps));
+    if (LAYER) {
+        e = make_map(&mp->v, a.q, bf16, 5, d5, box_row5, false);
+        if (e == cudaSuccess && bf16) e = make_map(&mp->q, a.q, true, 5, d5, box_half, true);
+    } else {
+        e = make_map(&mp->v, a.v, bf16, 4, d4, box_row4, false);
+        if (e == cudaSuccess && bf16) e = make_map(&mp->q, a.q, true, 4, d4, box_half4, true);
+        if (e == cudaSuccess && bf16) e = make_map(&mp->k, a.k, true, 4, d4, box_half4, true);
+    }
+    if (e == cudaSuccess && bf16) e = make_map(&mp->alpha, a.alpha, false, 4, d4, box_al, true);
+    if (e == cudaSuccess) e = make_map(&mp->o, a.o, false, 4, d4, box_row4, false);
+    return e;
+}
+
 template <typename TQ, bool LAYER, bool NORM>
 cudaError_t launch_tc_typed(const PrefillArgs &a, cudaStream_t stream) {
-    auto kernel = kda_prefill_tc_kernel<TQ, LAYER, NORM>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    PrefillMaps mp;
+    cudaError_t e = make_maps<TQ, LAYER>(a, &mp);
     if (e != cudaSuccess) return e;
-    kernel<<<dim3(a.M * a.H), NT, SMEM_BYTES, stream>>>(a);
+    auto kernel = kda_prefill_tc_kernel<TQ, LAYER, NORM>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3(a.M * a.H), NT, SMEM_BYTES, stream>>>(a, mp);
     return cudaGetLastError();
 }
 

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for sm_100-class features used by the kernels:
-// mbarriers, bulk (TMA) copies global -> shared, named barriers, L2 cache
+// mbarriers, bulk and tiled-tensor (TMA) copies, named barriers, L2 cache
 // policies. Every mbarrier wait is bounded: it gives up after a clock64()
 // deadline and reports failure to the caller, which records an error and
 // returns instead of spinning forever.
@@ -101,6 +101,40 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Tiled tensor copies (TMA) through a tensor map made on the host with
+// cuTensorMapEncodeTiled and passed as a __grid_constant__ kernel parameter
+// (`tmap` is its address). Coordinates are element indices, innermost first;
+// the innermost one times the element size must be a multiple of 16 bytes,
+// and none may be negative for a store. A load always transfers the whole box
+// (parts outside the tensor read as zero) and completes the box's bytes on
+// `bar`; a store writes only the parts inside the tensor and is tracked by the
+// issuing thread's bulk async-groups (bulk_commit / bulk_wait_*).
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_t *bar, int x, int y,
+                                            int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void *dst, const void *tmap, uint64_t *bar, int x, int y,
+                                            int z, int w, int u) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "r"(u)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const void *tmap, const void *src, int x, int y, int z,
+                                             int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
 }
 
 // Prefetch [src, src + bytes) into L2 (no shared memory involved).
