@@ -175,14 +175,13 @@ __device__ __forceinline__ float lg2(float x) {
     return y;
 }
 
-// FP32 -> TF32, round to nearest (ties away from zero), by adding half a
-// TF32 ulp to the magnitude bits and clearing the 13 bits TF32 drops. The
-// tensor cores read an FP32 operand as TF32 by ignoring those bits, a biased
-// truncation; operands written here are rounded first so their errors stay
-// unbiased. (Inputs are finite; nothing here rounds into inf or NaN.)
-__device__ __forceinline__ float tf32r(float x) {
-    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
-}
+// An FP32 operand prepared for a TF32 product: the tensor cores read it by
+// dropping its 13 low mantissa bits (a biased truncation, pinned by the tensor
+// core tests), so adding half a TF32 ulp to the magnitude bits first makes
+// that a round to nearest (ties away from zero) and the errors unbiased. The
+// low bits are left for the hardware to drop. (Inputs are finite; nothing
+// here rounds into inf or NaN.)
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(__float_as_uint(x) + 0x1000u); }
 
 __device__ __forceinline__ void st_tile4(unsigned char *tile, uint32_t row, uint32_t c4,
                                          uint32_t kbytes, float a, float b, float c, float d) {
@@ -570,16 +569,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             const float4 kb = *reinterpret_cast<const float4 *>(sNorm + (64 + r) * LDN + 4);
             const float sq = qa.x + qa.y + qa.z + qa.w + qb.x + qb.y + qb.z + qb.w + kL2Eps;
             const float sk = ka.x + ka.y + ka.z + ka.w + kb.x + kb.y + kb.z + kb.w + kL2Eps;
-            // The layer form takes the hardware reciprocal square root (a few
-            // ulp, far inside the TF32 operand error); the plain form keeps
-            // the correctly rounded one, which schedules without spills there.
-            if constexpr (LAYER) {
-                rq[g] = rsqrtf(sq);
-                rk[g] = rsqrtf(sk);
-            } else {
-                rq[g] = 1.0f / sqrtf(sq);
-                rk[g] = 1.0f / sqrtf(sk);
-            }
+            // the hardware reciprocal square root: a few ulp, far inside the
+            // TF32 operand error
+            rq[g] = rsqrtf(sq);
+            rk[g] = rsqrtf(sk);
         }
         // per-channel factors (log2 units):
         //   half 0: u = e^{G - G_15};  R0o = K e^{m_1 - G} with m_1 = G_31 + L_47
@@ -709,21 +702,18 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                      Lq[g][2] * em[2], Lq[g][3] * em[3]);
             // Kdec^T tile (row = key channel, K = token): a 4 x 4 transpose among
             // lanes rr = 4 hh .. 4 hh + 3, after which lane (hh, ce) holds channel
-            // 4 c4 + ce of tokens 8 g + 4 hh .. + 3. Step i: lane sends its element
-            // (ce - i) % 4 and receives token position (ce + i) % 4.
+            // 4 c4 + ce of tokens 8 g + 4 hh .. + 3. Two butterfly stages: the
+            // off-diagonal 2 x 2 blocks swap between lanes ce and ce ^ 2, then
+            // each 2 x 2 block transposes between lanes ce and ce ^ 1.
             const int ce = rr & 3, hh = rr >> 2;
+            const bool b1 = ce & 2, b0 = ce & 1;
             const float kc[4] = {Rk[g][0] * ed[0], Rk[g][1] * ed[1], Rk[g][2] * ed[2], Rk[g][3] * ed[3]};
-            float ko[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int es = (ce - i) & 3, pos = (ce + i) & 3;
-                const float send = es == 0 ? kc[0] : (es == 1 ? kc[1] : (es == 2 ? kc[2] : kc[3]));
-                const float recv = __shfl_sync(0xffffffffu, send, 8 * qq + 4 * hh + pos);
-                ko[0] = pos == 0 ? recv : ko[0];
-                ko[1] = pos == 1 ? recv : ko[1];
-                ko[2] = pos == 2 ? recv : ko[2];
-                ko[3] = pos == 3 ? recv : ko[3];
-            }
+            float r0 = __shfl_xor_sync(0xffffffffu, b1 ? kc[0] : kc[2], 2);
+            float r1 = __shfl_xor_sync(0xffffffffu, b1 ? kc[1] : kc[3], 2);
+            const float v4[4] = {b1 ? r0 : kc[0], b1 ? r1 : kc[1], b1 ? kc[2] : r0, b1 ? kc[3] : r1};
+            r0 = __shfl_xor_sync(0xffffffffu, b0 ? v4[0] : v4[1], 1);
+            r1 = __shfl_xor_sync(0xffffffffu, b0 ? v4[2] : v4[3], 1);
+            const float ko[4] = {b0 ? r0 : v4[0], b0 ? v4[1] : r0, b0 ? r1 : v4[2], b0 ? v4[3] : r1};
             st_tile4(sm + T_KDEC, 4 * c4 + ce, 8 * rh + 2 * g + hh, KB64, ko[0], ko[1], ko[2], ko[3]);
         }
         umma::fence_smem_to_async();
@@ -881,9 +871,18 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         {  // S^T[j][c] *= e^{G63_c}
             float s32[32];
             umma::ld_x32(tq + TM_S + 32 * hq, s32);
+            const float4 *gam4 = reinterpret_cast<const float4 *>(sGam + 32 * hq);
             umma::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) s32[e] *= sGam[32 * hq + e];
+            for (int e = 0; e < 8; ++e) {
+                const float4 g4 = gam4[e];
+                const float2 a = __fmul2_rn(make_float2(s32[4 * e], s32[4 * e + 1]), make_float2(g4.x, g4.y));
+                const float2 b = __fmul2_rn(make_float2(s32[4 * e + 2], s32[4 * e + 3]), make_float2(g4.z, g4.w));
+                s32[4 * e] = a.x;
+                s32[4 * e + 1] = a.y;
+                s32[4 * e + 2] = b.x;
+                s32[4 * e + 3] = b.y;
+            }
             umma::st_x32(tq + TM_S + 32 * hq, s32);
         }
         umma::wait_st();
