@@ -139,6 +139,11 @@ constexpr int kLoader = 32 * kVWarp;
 // named barriers (0 is __syncthreads): the issuer waits for all threads,
 // the others only signal and move on
 constexpr uint32_t kBarMma1 = 1, kBarMma3 = 2, kBarOut = 3;
+// the plain form splits the CTA in phase 5: warps 0-7 take the inverse
+// (their own barrier), warps 8-15 meanwhile the state-pass work of phase 6
+// (in the layer form that work carries the v conv and stays after the
+// inverse, on all warps)
+constexpr uint32_t kBarInv = 4;
 
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_D3 = 128, TM_Z = 256, TM_D4 = 320, TM_D1 = 384;
@@ -733,159 +738,173 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         if (!kTma && c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
 
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
-        // (runs on CUDA cores while MMA3 is on the tensor cores; v of this
-        // chunk is loaded meanwhile)
-
-        // 5a. diagonal 16 x 16 blocks, one lane per column: T_bb = (I + A_bb)^-1
-        if (warp < 2) {
-            const int b = 2 * warp + (lane >> 4), jj = lane & 15, j0 = 16 * b;
-            float tcol[16];
+        // (on CUDA cores while MMA3 runs on the tensor cores; split form: warps
+        // 0-7 only, while warps 8-15 take phase 6 as soon as MMA3 is done)
+        constexpr bool kSplit = !LAYER;
+        constexpr int kInvThreads = kSplit ? 256 : NT;
+        auto inv_sync = [&]() {
+            if (kSplit) ptx::named_bar_sync(kBarInv, kInvThreads);
+            else __syncthreads();
+        };
+        if (warp < kInvThreads / 32) {
+            // 5a. diagonal 16 x 16 blocks, one lane per column: T_bb = (I + A_bb)^-1
+            if (warp < 2) {
+                const int b = 2 * warp + (lane >> 4), jj = lane & 15, j0 = 16 * b;
+                float tcol[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float x0 = r == jj ? 1.f : 0.f, x1 = 0.f;
+                for (int r = 0; r < 16; ++r) {
+                    float x0 = r == jj ? 1.f : 0.f, x1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; i += 2) {
-                    x0 = fmaf(-sA[(j0 + r) * LDA + j0 + i], tcol[i], x0);
-                    if (i + 1 < r) x1 = fmaf(-sA[(j0 + r) * LDA + j0 + i + 1], tcol[i + 1], x1);
+                    for (int i = 0; i < r; i += 2) {
+                        x0 = fmaf(-sA[(j0 + r) * LDA + j0 + i], tcol[i], x0);
+                        if (i + 1 < r) x1 = fmaf(-sA[(j0 + r) * LDA + j0 + i + 1], tcol[i + 1], x1);
+                    }
+                    tcol[r] = r >= jj ? x0 + x1 : 0.f;
                 }
-                tcol[r] = r >= jj ? x0 + x1 : 0.f;
-            }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(j0 + r) * LDA + j0 + jj] = tcol[r];
-        }
-        __syncthreads();
-        // 5b. off-diagonal blocks, level d = R - I at a time:
-        //     T_RI = -T_RR X_RI,  X_RI = sum_{Q=I}^{R-1} A_RQ T_QI
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            // unit: block I (R = I + d), row r16, four columns 4 q16 .. + 3
-            const int I = tid >> 6, r16 = (tid >> 2) & 15, q16 = tid & 3, Rb = I + d;
-            if (I < nblk) {
-                float x4[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int Q = I; Q < Rb; ++Q) {
+                for (int r = 0; r < 16; ++r) sT[(j0 + r) * LDA + j0 + jj] = tcol[r];
+            }
+            inv_sync();
+            // 5b. off-diagonal blocks, level d = R - I at a time:
+            //     T_RI = -T_RR X_RI,  X_RI = sum_{Q=I}^{R-1} A_RQ T_QI
+            for (int d = 1; d < 4; ++d) {
+                const int nblk = 4 - d;
+                // unit: block I (R = I + d), row r16, four columns 4 q16 .. + 3
+                const int I = tid >> 6, r16 = (tid >> 2) & 15, q16 = tid & 3, Rb = I + d;
+                if (I < nblk) {
+                    float x4[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int Q = I; Q < Rb; ++Q) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float av = sA[(16 * Rb + r16) * LDA + 16 * Q + t];
+                            const float4 tv =
+                                *reinterpret_cast<const float4 *>(sT + (16 * Q + t) * LDA + 16 * I + 4 * q16);
+                            x4[0] = fmaf(av, tv.x, x4[0]);
+                            x4[1] = fmaf(av, tv.y, x4[1]);
+                            x4[2] = fmaf(av, tv.z, x4[2]);
+                            x4[3] = fmaf(av, tv.w, x4[3]);
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(sX + (I * 16 + r16) * 16 + 4 * q16) =
+                        make_float4(x4[0], x4[1], x4[2], x4[3]);
+                }
+                inv_sync();
+                if (I < nblk) {
+                    float t4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
-                        const float av = sA[(16 * Rb + r16) * LDA + 16 * Q + t];
-                        const float4 tv =
-                            *reinterpret_cast<const float4 *>(sT + (16 * Q + t) * LDA + 16 * I + 4 * q16);
-                        x4[0] = fmaf(av, tv.x, x4[0]);
-                        x4[1] = fmaf(av, tv.y, x4[1]);
-                        x4[2] = fmaf(av, tv.z, x4[2]);
-                        x4[3] = fmaf(av, tv.w, x4[3]);
+                        const float tv = sT[(16 * Rb + r16) * LDA + 16 * Rb + t];
+                        const float4 xv = *reinterpret_cast<const float4 *>(sX + (I * 16 + t) * 16 + 4 * q16);
+                        t4[0] = fmaf(tv, xv.x, t4[0]);
+                        t4[1] = fmaf(tv, xv.y, t4[1]);
+                        t4[2] = fmaf(tv, xv.z, t4[2]);
+                        t4[3] = fmaf(tv, xv.w, t4[3]);
                     }
+                    *reinterpret_cast<float4 *>(sT + (16 * Rb + r16) * LDA + 16 * I + 4 * q16) =
+                        make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
                 }
-                *reinterpret_cast<float4 *>(sX + (I * 16 + r16) * 16 + 4 * q16) =
-                    make_float4(x4[0], x4[1], x4[2], x4[3]);
+                inv_sync();
             }
-            __syncthreads();
-            if (I < nblk) {
-                float t4[4] = {0.f, 0.f, 0.f, 0.f};
+            // 5c. M[r][i] = T[r][i] beta_i (lower with diagonal) into the operand tile
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float tv = sT[(16 * Rb + r16) * LDA + 16 * Rb + t];
-                    const float4 xv = *reinterpret_cast<const float4 *>(sX + (I * 16 + t) * 16 + 4 * q16);
-                    t4[0] = fmaf(tv, xv.x, t4[0]);
-                    t4[1] = fmaf(tv, xv.y, t4[1]);
-                    t4[2] = fmaf(tv, xv.z, t4[2]);
-                    t4[3] = fmaf(tv, xv.w, t4[3]);
+            for (int it = 0; it < 1024 / kInvThreads; ++it) {
+                const int u = it * kInvThreads + tid;
+                const int r = 8 * (u >> 7) + (u & 7), iq = (u >> 3) & 15, i = 4 * iq;
+                const float4 tv = *reinterpret_cast<const float4 *>(sT + r * LDA + i);
+                const float4 bv = *reinterpret_cast<const float4 *>(sBeta + i);
+                st_tile4(sm + T_M, r, iq, KB64, i <= r ? tv.x * bv.x : 0.f, i + 1 <= r ? tv.y * bv.y : 0.f,
+                         i + 2 <= r ? tv.z * bv.z : 0.f, i + 3 <= r ? tv.w * bv.w : 0.f);
+            }
+            umma::fence_smem_to_async();
+            // the next chunk's beta (sBeta of this chunk has been read)
+            if (tid < C) {
+                const int t = c0 + C + tid;
+                beta_n = t < T ? __ldg(a.beta + ((size_t)m * T + t) * a.H + h) : 0.f;
+            }
+        }
+        if (!kSplit || warp >= kInvThreads / 32) {
+            // ------------------------------------------------------ 6. Z = V - Y, decay S
+            // split form: warps 8-15 while warps 0-7 invert, warp w doing the
+            // units hq6 = 2 ((w - 8) / 4) and + 1 of its lane quarter; else
+            // every warp its unit hq6 = hq
+            if (!ptx::mbar_wait(&bar[1], phase, kWaitBudget)) {
+                raise_error(2u);
+                ok = false;
+                break;
+            }
+            umma::fence_after_sync();
+            // MMA3 has read [Kd; Qd]: the region takes the next chunk's q, k, alpha
+            if (kTma && tid == kLoader && c0 + C < T) issue_qka(c0 + C);
+            if (!ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
+                raise_error(16u);
+                ok = false;
+                break;
+            }
+#pragma unroll 1
+            for (int u6 = 0; u6 < (kSplit ? 2 : 1); ++u6) {
+                const int hq6 = kSplit ? 2 * ((warp - 8) >> 2) + u6 : hq;
+                {
+                    // v of tokens 16 hq6 .. + 15 at channel j from the staged chunk (0 past T)
+                    float vf[16];
+                    if constexpr (LAYER) {  // conv over tokens 16 hq6 - 3 .. 16 hq6 + 15 (the 3 before the chunk kept aside)
+                        const float *vc = sVc + ((c0 / C + 1) & 1) * 3 * DK;
+                        float raw[19];
+#pragma unroll
+                        for (int i = 0; i < 19; ++i) {
+                            const int tl = 16 * hq6 - 3 + i;  // token within the chunk
+                            raw[i] = tl < 0 ? vc[(tl + 3) * DK + j]
+                                            : (c0 + tl < T ? RW::widen1(reinterpret_cast<const typename RW::V1 *>(sV)[tl * DK + j]) : 0.f);
+                        }
+                        if (hq6 == 3) {  // raw v of tokens 61-63, for the next chunk
+                            float *vn = sVc + ((c0 / C) & 1) * 3 * DK;
+#pragma unroll
+                            for (int tap = 0; tap < 3; ++tap) vn[tap * DK + j] = raw[16 + tap];
+                        }
+                        const float4 wv = sWqk[2 * DK + j];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float pre = wv.x * raw[i] + wv.y * raw[i + 1] + wv.z * raw[i + 2] + wv.w * raw[i + 3];
+                            vf[i] = c0 + 16 * hq6 + i < T ? __fdividef(pre, 1.0f + __expf(-pre)) : 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int tl = 16 * hq6 + e;
+                            vf[e] = c0 + tl < T ? RW::widen1(reinterpret_cast<const typename RW::V1 *>(sV)[tl * DK + j]) : 0.f;
+                        }
+                    }
+                    float y[16];  // tokens 16 hq6 .. 16 hq6 + 15
+                    umma::ld_x16(tq + TM_D3 + 16 * hq6, y);
+                    umma::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) y[e] = tf32r(vf[e] - y[e]);
+                    umma::st_x16(tq + TM_Z + 16 * hq6, y);
                 }
-                *reinterpret_cast<float4 *>(sT + (16 * Rb + r16) * LDA + 16 * I + 4 * q16) =
-                    make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
-            }
-            __syncthreads();
-        }
-        // 5c. M[r][i] = T[r][i] beta_i (lower with diagonal) into the operand tile
+                {  // S^T[j][c] *= e^{G63_c}
+                    float s32[32];
+                    umma::ld_x32(tq + TM_S + 32 * hq6, s32);
+                    const float4 *gam4 = reinterpret_cast<const float4 *>(sGam + 32 * hq6);
+                    umma::wait_ld();
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int u = it * NT + tid;
-            const int r = 8 * (u >> 7) + (u & 7), iq = (u >> 3) & 15, i = 4 * iq;
-            const float4 tv = *reinterpret_cast<const float4 *>(sT + r * LDA + i);
-            const float4 bv = *reinterpret_cast<const float4 *>(sBeta + i);
-            st_tile4(sm + T_M, r, iq, KB64, i <= r ? tv.x * bv.x : 0.f, i + 1 <= r ? tv.y * bv.y : 0.f,
-                     i + 2 <= r ? tv.z * bv.z : 0.f, i + 3 <= r ? tv.w * bv.w : 0.f);
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 g4 = gam4[e];
+                        const float2 a = __fmul2_rn(make_float2(s32[4 * e], s32[4 * e + 1]), make_float2(g4.x, g4.y));
+                        const float2 b = __fmul2_rn(make_float2(s32[4 * e + 2], s32[4 * e + 3]), make_float2(g4.z, g4.w));
+                        s32[4 * e] = a.x;
+                        s32[4 * e + 1] = a.y;
+                        s32[4 * e + 2] = b.x;
+                        s32[4 * e + 3] = b.y;
+                    }
+                    umma::st_x32(tq + TM_S + 32 * hq6, s32);
+                }
+            }
+            umma::wait_st();
         }
-        umma::fence_smem_to_async();
-        // the next chunk's beta (sBeta of this chunk has been read)
-        if (tid < C) {
-            const int t = c0 + C + tid;
-            beta_n = t < T ? __ldg(a.beta + ((size_t)m * T + t) * a.H + h) : 0.f;
-        }
-
-        // ---------------------------------------------------------- 6. Z = V - Y, decay S
-        if (!ptx::mbar_wait(&bar[1], phase, kWaitBudget)) {
-            raise_error(2u);
-            ok = false;
-            break;
-        }
-        umma::fence_after_sync();
-        // MMA3 has read [Kd; Qd]: the region takes the next chunk's q, k, alpha
         if (kTma && c0 + C < T) {
-            if (tid == kLoader) issue_qka(c0 + C);
             qka_pending = 1;
             qka_parity = phase ^ 1;
         }
-        if (ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
-            v_pending = 0;
-        } else {
-            raise_error(16u);
-            ok = false;
-            break;
-        }
-        {
-            // v of tokens 16 hq .. + 15 at channel j from the staged chunk (0 past T)
-            float vf[16];
-            if constexpr (LAYER) {  // conv over tokens 16 hq - 3 .. 16 hq + 15 (the 3 before the chunk kept aside)
-                const float *vc = sVc + ((c0 / C + 1) & 1) * 3 * DK;
-                float raw[19];
-#pragma unroll
-                for (int i = 0; i < 19; ++i) {
-                    const int tl = 16 * hq - 3 + i;  // token within the chunk
-                    raw[i] = tl < 0 ? vc[(tl + 3) * DK + j]
-                                    : (c0 + tl < T ? RW::widen1(reinterpret_cast<const typename RW::V1 *>(sV)[tl * DK + j]) : 0.f);
-                }
-                if (hq == 3) {  // raw v of tokens 61-63, for the next chunk
-                    float *vn = sVc + ((c0 / C) & 1) * 3 * DK;
-#pragma unroll
-                    for (int tap = 0; tap < 3; ++tap) vn[tap * DK + j] = raw[16 + tap];
-                }
-                const float4 wv = sWqk[2 * DK + j];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float pre = wv.x * raw[i] + wv.y * raw[i + 1] + wv.z * raw[i + 2] + wv.w * raw[i + 3];
-                    vf[i] = c0 + 16 * hq + i < T ? __fdividef(pre, 1.0f + __expf(-pre)) : 0.f;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int tl = 16 * hq + e;
-                    vf[e] = c0 + tl < T ? RW::widen1(reinterpret_cast<const typename RW::V1 *>(sV)[tl * DK + j]) : 0.f;
-                }
-            }
-            float y[16];  // tokens 16 hq .. 16 hq + 15
-            umma::ld_x16(tq + TM_D3 + 16 * hq, y);
-            umma::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) y[e] = tf32r(vf[e] - y[e]);
-            umma::st_x16(tq + TM_Z + 16 * hq, y);
-        }
-        {  // S^T[j][c] *= e^{G63_c}
-            float s32[32];
-            umma::ld_x32(tq + TM_S + 32 * hq, s32);
-            const float4 *gam4 = reinterpret_cast<const float4 *>(sGam + 32 * hq);
-            umma::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float4 g4 = gam4[e];
-                const float2 a = __fmul2_rn(make_float2(s32[4 * e], s32[4 * e + 1]), make_float2(g4.x, g4.y));
-                const float2 b = __fmul2_rn(make_float2(s32[4 * e + 2], s32[4 * e + 3]), make_float2(g4.z, g4.w));
-                s32[4 * e] = a.x;
-                s32[4 * e + 1] = a.y;
-                s32[4 * e + 2] = b.x;
-                s32[4 * e + 3] = b.y;
-            }
-            umma::st_x32(tq + TM_S + 32 * hq, s32);
-        }
-        umma::wait_st();
+        v_pending = 0;
         // the layer form: raw q, k of tokens 29-31 of the next chunk (loaded in phase 4)
         if (!kTma && LAYER && rh == 0 && rr >= 5 && c0 + C < T) {
             float xq[4], xk[4];
