@@ -280,13 +280,6 @@ __device__ __forceinline__ void fetch_qka(QKA<__nv_bfloat16> &R, const unsigned 
         R.al[g] = *reinterpret_cast<const float4 *>(sm + ST_AL + (c4 >> 3) * BOX + swz(r, (c4 & 7) * 16));
     }
 }
-// One staged raw BF16 value: tensor X (0 q, 1 k), token row, channel c.
-__device__ __forceinline__ float staged1(const unsigned char *sm, int X, int row, int c) {
-    const unsigned short u =
-        *reinterpret_cast<const unsigned short *>(sm + (X ? ST_K : ST_Q) + (c >> 6) * BOX + swz(row, (c & 63) * 2));
-    return __uint_as_float((uint32_t)u << 16);
-}
-
 template <typename TQ, bool LAYER, bool NORM>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ PrefillMaps mp) {
     // BF16 q, k arrive by tensor copies into shared memory; FP32 ones (twice
@@ -461,45 +454,75 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                     G[g][e] = t < T ? __fdividef(lbl2, 1.0f + __expf(-z)) : 0.f;
                 }
             }
-            // conv + SiLU, token groups from last to first (each reads the raw
-            // values of the group before it): token 8 g + rr - kk sits in lane
-            // rr - kk of group g, or in lane rr - kk + 8 of group g - 1, or (first
-            // group) in the buffer of the three tokens before the half, at tap
-            // rr - kk + 3
-            const float *xp = rh ? sXa : sXb + ((cidx + 1) & 1) * XB_F;
+            if constexpr (kTma) {
+                // conv + SiLU with the raw taps (tokens t - 1, t - 2, t - 3) read from the
+                // staged boxes; rows before the chunk from the previous chunk's last three
+                const float *xp = sXb + ((cidx + 1) & 1) * XB_F;
 #pragma unroll
-            for (int g = 3; g >= 0; --g) {
-                const int t = c0 + 32 * rh + 8 * g + rr;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float wq3[3], wk3[3];  // tokens t - 1, t - 2, t - 3
+                for (int g = 0; g < 4; ++g) {
+                    const int t = c0 + 32 * rh + 8 * g + rr;
+                    float tq3[3][4], tk3[3][4];
 #pragma unroll
                     for (int kk = 1; kk <= 3; ++kk) {
-                        const int src = 8 * qq + ((rr - kk) & 7);
-                        const float aq = __shfl_sync(0xffffffffu, qf[g][e], src);
-                        const float ak = __shfl_sync(0xffffffffu, kf[g][e], src);
-                        float bq, bk;
-                        if (g > 0) {
-                            bq = __shfl_sync(0xffffffffu, qf[g > 0 ? g - 1 : 0][e], src);
-                            bk = __shfl_sync(0xffffffffu, kf[g > 0 ? g - 1 : 0][e], src);
-                        } else if (kTma && rh == 1) {  // tokens 29-31 from the staged boxes
-                            const int tap = rr - kk + 3 < 2 ? rr - kk + 3 : 2;  // used only when rr < kk
-                            bq = staged1(sm, 0, 29 + tap, 4 * c4 + e);
-                            bk = staged1(sm, 1, 29 + tap, 4 * c4 + e);
-                        } else {
-                            const int tap = rr - kk + 3 < 2 ? rr - kk + 3 : 2;  // used only when rr < kk
-                            bq = xp[(0 * 3 + tap) * DK + 4 * c4 + e];
-                            bk = xp[(1 * 3 + tap) * DK + 4 * c4 + e];
+                        const int row = 32 * rh + 8 * g + rr - kk;
+                        const uint32_t off = (c4 >> 4) * BOX + swz(row < 0 ? 0 : row, (c4 & 15) * 8);
+                        RW::widen4(*reinterpret_cast<const uint2 *>(sm + ST_Q + off), tq3[kk - 1]);
+                        RW::widen4(*reinterpret_cast<const uint2 *>(sm + ST_K + off), tk3[kk - 1]);
+                        if (row < 0) {  // tap row + 3 of the previous chunk's tokens 61-63
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                tq3[kk - 1][e] = xp[(0 * 3 + row + 3) * DK + 4 * c4 + e];
+                                tk3[kk - 1][e] = xp[(1 * 3 + row + 3) * DK + 4 * c4 + e];
+                            }
                         }
-                        wq3[kk - 1] = rr >= kk ? aq : bq;
-                        wk3[kk - 1] = rr >= kk ? ak : bk;
                     }
-                    const float4 wq = sWqk[4 * c4 + e], wk = sWqk[DK + 4 * c4 + e];
-                    const float pre_q = wq.x * wq3[2] + wq.y * wq3[1] + wq.z * wq3[0] + wq.w * qf[g][e];
-                    const float pre_k = wk.x * wk3[2] + wk.y * wk3[1] + wk.z * wk3[0] + wk.w * kf[g][e];
-                    const bool live = t < T;  // tokens past T stay out of the chunk
-                    qf[g][e] = live ? __fdividef(pre_q, 1.0f + __expf(-pre_q)) : 0.f;
-                    kf[g][e] = live ? __fdividef(pre_k, 1.0f + __expf(-pre_k)) : 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 wq = sWqk[4 * c4 + e], wk = sWqk[DK + 4 * c4 + e];
+                        const float pre_q = wq.x * tq3[2][e] + wq.y * tq3[1][e] + wq.z * tq3[0][e] + wq.w * qf[g][e];
+                        const float pre_k = wk.x * tk3[2][e] + wk.y * tk3[1][e] + wk.z * tk3[0][e] + wk.w * kf[g][e];
+                        const bool live = t < T;  // tokens past T stay out of the chunk
+                        qf[g][e] = live ? __fdividef(pre_q, 1.0f + __expf(-pre_q)) : 0.f;
+                        kf[g][e] = live ? __fdividef(pre_k, 1.0f + __expf(-pre_k)) : 0.f;
+                    }
+                }
+            } else {
+                // conv + SiLU, token groups from last to first (each reads the raw
+                // values of the group before it): token 8 g + rr - kk sits in lane
+                // rr - kk of group g, or in lane rr - kk + 8 of group g - 1, or (first
+                // group) in the buffer of the three tokens before the half, at tap
+                // rr - kk + 3
+                const float *xp = rh ? sXa : sXb + ((cidx + 1) & 1) * XB_F;
+#pragma unroll
+                for (int g = 3; g >= 0; --g) {
+                    const int t = c0 + 32 * rh + 8 * g + rr;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float wq3[3], wk3[3];  // tokens t - 1, t - 2, t - 3
+#pragma unroll
+                        for (int kk = 1; kk <= 3; ++kk) {
+                            const int src = 8 * qq + ((rr - kk) & 7);
+                            const float aq = __shfl_sync(0xffffffffu, qf[g][e], src);
+                            const float ak = __shfl_sync(0xffffffffu, kf[g][e], src);
+                            float bq, bk;
+                            if (g > 0) {
+                                bq = __shfl_sync(0xffffffffu, qf[g > 0 ? g - 1 : 0][e], src);
+                                bk = __shfl_sync(0xffffffffu, kf[g > 0 ? g - 1 : 0][e], src);
+                            } else {
+                                const int tap = rr - kk + 3 < 2 ? rr - kk + 3 : 2;  // used only when rr < kk
+                                bq = xp[(0 * 3 + tap) * DK + 4 * c4 + e];
+                                bk = xp[(1 * 3 + tap) * DK + 4 * c4 + e];
+                            }
+                            wq3[kk - 1] = rr >= kk ? aq : bq;
+                            wk3[kk - 1] = rr >= kk ? ak : bk;
+                        }
+                        const float4 wq = sWqk[4 * c4 + e], wk = sWqk[DK + 4 * c4 + e];
+                        const float pre_q = wq.x * wq3[2] + wq.y * wq3[1] + wq.z * wq3[0] + wq.w * qf[g][e];
+                        const float pre_k = wk.x * wk3[2] + wk.y * wk3[1] + wk.z * wk3[0] + wk.w * kf[g][e];
+                        const bool live = t < T;  // tokens past T stay out of the chunk
+                        qf[g][e] = live ? __fdividef(pre_q, 1.0f + __expf(-pre_q)) : 0.f;
+                        kf[g][e] = live ? __fdividef(pre_k, 1.0f + __expf(-pre_k)) : 0.f;
+                    }
                 }
             }
         } else {
