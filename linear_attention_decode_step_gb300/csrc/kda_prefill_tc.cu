@@ -174,6 +174,16 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// SiLU(x) = x sigmoid(x) with sigmoid(x) = (1 + tanh(x / 2)) / 2, i.e.
+// h + h tanh(h) for h = x / 2: one hardware tanh (tanh.approx.f32, relative
+// error about 2^-11) in place of an exponential and a reciprocal, the
+// special-function pipe being what bounds the conv of the layer form
+__device__ __forceinline__ float silu(float x) {
+    const float h = 0.5f * x;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -482,8 +492,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                         const float pre_q = wq.x * tq3[2][e] + wq.y * tq3[1][e] + wq.z * tq3[0][e] + wq.w * qf[g][e];
                         const float pre_k = wk.x * tk3[2][e] + wk.y * tk3[1][e] + wk.z * tk3[0][e] + wk.w * kf[g][e];
                         const bool live = t < T;  // tokens past T stay out of the chunk
-                        qf[g][e] = live ? __fdividef(pre_q, 1.0f + __expf(-pre_q)) : 0.f;
-                        kf[g][e] = live ? __fdividef(pre_k, 1.0f + __expf(-pre_k)) : 0.f;
+                        qf[g][e] = live ? silu(pre_q) : 0.f;
+                        kf[g][e] = live ? silu(pre_k) : 0.f;
                     }
                 }
             } else {
@@ -520,8 +530,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                         const float pre_q = wq.x * wq3[2] + wq.y * wq3[1] + wq.z * wq3[0] + wq.w * qf[g][e];
                         const float pre_k = wk.x * wk3[2] + wk.y * wk3[1] + wk.z * wk3[0] + wk.w * kf[g][e];
                         const bool live = t < T;  // tokens past T stay out of the chunk
-                        qf[g][e] = live ? __fdividef(pre_q, 1.0f + __expf(-pre_q)) : 0.f;
-                        kf[g][e] = live ? __fdividef(pre_k, 1.0f + __expf(-pre_k)) : 0.f;
+                        qf[g][e] = live ? silu(pre_q) : 0.f;
+                        kf[g][e] = live ? silu(pre_k) : 0.f;
                     }
                 }
             }
@@ -887,7 +897,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float pre = wv.x * raw[i] + wv.y * raw[i + 1] + wv.z * raw[i + 2] + wv.w * raw[i + 3];
-                            vf[i] = c0 + 16 * hq6 + i < T ? __fdividef(pre, 1.0f + __expf(-pre)) : 0.f;
+                            vf[i] = c0 + 16 * hq6 + i < T ? silu(pre) : 0.f;
                         }
                     } else {
 #pragma unroll
@@ -965,6 +975,18 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
             umma::commit(&bar[3]);
         }
+        // the norm's output gate rows of this warp (4 w .. 4 w + 3) and weights, loaded
+        // under the state-pass products
+        float4 og[4], nw;
+        if (NORM) {
+            nw = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * warp + i;
+                og[i] = c0 + t < T ? __ldg(reinterpret_cast<const float4 *>(a.out_gate + (((size_t)m * T + c0 + t) * a.H + h) * DK) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         if (!ptx::mbar_wait(&bar[3], phase, kWaitBudget)) {
             raise_error(8u);
             ok = false;
@@ -983,7 +1005,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         if (NORM) {  // y = o / sqrt(mean o^2 + eps) * w * sigmoid(gate), warp w: rows 4 w .. 4 w + 3
             __syncthreads();
-            const float4 nw = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t = 4 * warp + i;
@@ -993,9 +1014,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 const float rn = rsqrtf(ss * (1.0f / DK) + a.norm_eps);
-                float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (c0 + t < T)
-                    g4 = __ldg(reinterpret_cast<const float4 *>(a.out_gate + (((size_t)m * T + c0 + t) * a.H + h) * DK) + lane);
+                const float4 g4 = og[i];
                 o4.x = o4.x * rn * nw.x / (1.0f + __expf(-g4.x));
                 o4.y = o4.y * rn * nw.y / (1.0f + __expf(-g4.y));
                 o4.z = o4.z * rn * nw.z / (1.0f + __expf(-g4.z));
