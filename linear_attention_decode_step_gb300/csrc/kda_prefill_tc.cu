@@ -85,20 +85,22 @@ constexpr uint32_t KB64 = C * 4;    // one row of a K = 64 tile
 constexpr uint32_t T_LA = 0;                       // [L0; Lq0; L1; Lq1]  128 x 128
 constexpr uint32_t T_RB = T_LA + 128 * KB128;      // [R0; R1; R0o]        96 x 128
 constexpr uint32_t PH1_END = T_RB + 96 * KB128;    // 114688
-// phase-2 tiles (overlay phase-1 once MMA1 has completed)
+// phase-2 tiles: [Kd; Qd], P, M, A, T and the inverse's scratch overlay the
+// phase-1 tiles once MMA1 has completed; Kdec^T lies past them and is written
+// while MMA1 runs
 constexpr uint32_t T_KQ = 0;                       // [Kd; Qd]       128 x 128
-constexpr uint32_t T_KDEC = T_KQ + 128 * KB128;    // Kdec^T          128 x 64
-constexpr uint32_t T_M = T_KDEC + 128 * KB64;      // M               64 x 64
-constexpr uint32_t T_P = T_M + 64 * KB64;          // P               64 x 64
-constexpr uint32_t T_A = T_P + 64 * KB64;          // A (plain [64][68] FP32)
+constexpr uint32_t T_P = T_KQ + 128 * KB128;       // P               64 x 64
+constexpr uint32_t T_M = T_P + 64 * KB64;          // M               64 x 64
+constexpr uint32_t T_A = T_M + 64 * KB64;          // A (plain [64][68] FP32)
 constexpr int LDA = 68;
 constexpr uint32_t T_T = T_A + 64 * LDA * 4;       // T = (I + A)^-1 (plain [64][68] FP32)
 constexpr uint32_t T_X = T_T + 64 * LDA * 4;       // scratch: up to 3 blocks of 16 x 16
-constexpr uint32_t T_V = T_X + 3 * 256 * 4;        // v of the chunk, token-major [64][128] (bulk copies)
+constexpr uint32_t T_KDEC = (T_X + 3 * 256 * 4 + 1023) / 1024 * 1024;  // Kdec^T  128 x 64
+constexpr uint32_t T_V = T_KDEC + 128 * KB64;      // v of the chunk, token-major [64][128] (tensor copies)
 constexpr uint32_t PH2_END = T_V + 64 * DK * 4;
-constexpr uint32_t T_O = T_A;                      // O staging [64][128]: phase 7 to the next chunk's phase 3, over A, T, X
-static_assert(64 * DK * 4 <= T_V - T_A, "O staging fits the A / T / X region");
-static_assert(T_A >= PH1_END, "A and P are written while nothing reads phase-1 tiles");
+constexpr uint32_t T_O = T_KDEC;                   // O staging [64][128]: phase 7 to the next chunk's MMA1, over Kdec^T
+static_assert(64 * DK * 4 <= T_V - T_O, "O staging fits the Kdec^T region");
+static_assert(T_KDEC >= PH1_END, "Kdec^T is written while MMA1 reads the phase-1 tiles");
 constexpr uint32_t TILES = PH2_END > PH1_END ? PH2_END : PH1_END;
 // small buffers (bytes)
 constexpr int LDN = 12;                            // norm partials row: 8 groups + 4 (bank shift)
@@ -139,11 +141,10 @@ constexpr int kLoader = 32 * kVWarp;
 // named barriers (0 is __syncthreads): the issuer waits for all threads,
 // the others only signal and move on
 constexpr uint32_t kBarMma1 = 1, kBarMma3 = 2, kBarOut = 3;
-// the plain form splits the CTA in phase 5: warps 0-7 take the inverse
-// (their own barrier), warps 8-15 meanwhile the state-pass work of phase 6
-// (in the layer form that work carries the v conv and stays after the
-// inverse, on all warps)
+// phase 5 splits the CTA: warps 0-7 take the inverse (their own barrier),
+// warps 8-15 meanwhile the state-pass work of phase 6
 constexpr uint32_t kBarInv = 4;
+constexpr int kInvThreads = 256;
 
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_D3 = 128, TM_Z = 256, TM_D4 = 320, TM_D1 = 384;
@@ -666,11 +667,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
-        // the previous chunk's O staging (over A, T, X, rewritten from phase 3 on)
-        // has been read by its bulk copies before MMA1 is issued
+        // the previous chunk's O staging (over Kdec^T, rewritten while MMA1 runs)
+        // has been read by its tensor store before anyone passes this barrier
         if (tid == 0 && c0 > 0) ptx::bulk_wait_read_all();
-        if (warp == kIssuer / 32) ptx::named_bar_sync(kBarMma1, NT);
-        else ptx::named_bar_arrive(kBarMma1, NT);
+        ptx::named_bar_sync(kBarMma1, NT);
         if (tid == kIssuer) {
             umma::fence_after_sync();
 #pragma unroll 1
@@ -679,6 +679,25 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                              umma::smem_desc(sbase + T_RB + ks * 256, 128, 8 * KB128), id96, ks > 0,
                              1);
             umma::commit(&bar[0]);
+        }
+        // under MMA1: Kdec = K e^{G63 - G} = R ed, as the Kdec^T tile
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            // Kdec^T tile (row = key channel, K = token): a 4 x 4 transpose among
+            // lanes rr = 4 hh .. 4 hh + 3, after which lane (hh, ce) holds channel
+            // 4 c4 + ce of tokens 8 g + 4 hh .. + 3. Two butterfly stages: the
+            // off-diagonal 2 x 2 blocks swap between lanes ce and ce ^ 2, then
+            // each 2 x 2 block transposes between lanes ce and ce ^ 1.
+            const int ce = rr & 3, hh = rr >> 2;
+            const bool b1 = ce & 2, b0 = ce & 1;
+            const float kc[4] = {Rk[g][0] * ed[0], Rk[g][1] * ed[1], Rk[g][2] * ed[2], Rk[g][3] * ed[3]};
+            float x0 = __shfl_xor_sync(0xffffffffu, b1 ? kc[0] : kc[2], 2);
+            float x1 = __shfl_xor_sync(0xffffffffu, b1 ? kc[1] : kc[3], 2);
+            const float v4[4] = {b1 ? x0 : kc[0], b1 ? x1 : kc[1], b1 ? kc[2] : x0, b1 ? kc[3] : x1};
+            x0 = __shfl_xor_sync(0xffffffffu, b0 ? v4[0] : v4[1], 1);
+            x1 = __shfl_xor_sync(0xffffffffu, b0 ? v4[2] : v4[3], 1);
+            const float ko[4] = {b0 ? x0 : v4[0], b0 ? v4[1] : x0, b0 ? x1 : v4[2], b0 ? v4[3] : x1};
+            st_tile4(sm + T_KDEC, 4 * c4 + ce, 8 * rh + 2 * g + hh, KB64, ko[0], ko[1], ko[2], ko[3]);
         }
         if (!ptx::mbar_wait(&bar[0], phase, kWaitBudget)) {
             raise_error(1u);
@@ -730,7 +749,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         __syncthreads();  // A, P visible; MMA1 operands may now be overwritten
 
         // ---------------------------------------------------------- 4. state-pass operands
-        //   Kd = K e^G = L em,   Qd = Lq em,   Kdec = K e^{G63 - G} = R ed
+        //   Kd = K e^G = L em,   Qd = Lq em   (Kdec^T was written under MMA1)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int r = r0 + 8 * g;
@@ -738,21 +757,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                      Lk[g][3] * em[3]);
             st_tile4(sm + T_KQ, 64 + r, c4, KB128, Lq[g][0] * em[0], Lq[g][1] * em[1],
                      Lq[g][2] * em[2], Lq[g][3] * em[3]);
-            // Kdec^T tile (row = key channel, K = token): a 4 x 4 transpose among
-            // lanes rr = 4 hh .. 4 hh + 3, after which lane (hh, ce) holds channel
-            // 4 c4 + ce of tokens 8 g + 4 hh .. + 3. Two butterfly stages: the
-            // off-diagonal 2 x 2 blocks swap between lanes ce and ce ^ 2, then
-            // each 2 x 2 block transposes between lanes ce and ce ^ 1.
-            const int ce = rr & 3, hh = rr >> 2;
-            const bool b1 = ce & 2, b0 = ce & 1;
-            const float kc[4] = {Rk[g][0] * ed[0], Rk[g][1] * ed[1], Rk[g][2] * ed[2], Rk[g][3] * ed[3]};
-            float r0 = __shfl_xor_sync(0xffffffffu, b1 ? kc[0] : kc[2], 2);
-            float r1 = __shfl_xor_sync(0xffffffffu, b1 ? kc[1] : kc[3], 2);
-            const float v4[4] = {b1 ? r0 : kc[0], b1 ? r1 : kc[1], b1 ? kc[2] : r0, b1 ? kc[3] : r1};
-            r0 = __shfl_xor_sync(0xffffffffu, b0 ? v4[0] : v4[1], 1);
-            r1 = __shfl_xor_sync(0xffffffffu, b0 ? v4[2] : v4[3], 1);
-            const float ko[4] = {b0 ? r0 : v4[0], b0 ? v4[1] : r0, b0 ? r1 : v4[2], b0 ? v4[3] : r1};
-            st_tile4(sm + T_KDEC, 4 * c4 + ce, 8 * rh + 2 * g + hh, KB64, ko[0], ko[1], ko[2], ko[3]);
         }
         umma::fence_smem_to_async();
         umma::fence_before_sync();
@@ -771,14 +775,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         if (!kTma && c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
 
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
-        // (on CUDA cores while MMA3 runs on the tensor cores; split form: warps
-        // 0-7 only, while warps 8-15 take phase 6 as soon as MMA3 is done)
-        constexpr bool kSplit = !LAYER;
-        constexpr int kInvThreads = kSplit ? 256 : NT;
-        auto inv_sync = [&]() {
-            if (kSplit) ptx::named_bar_sync(kBarInv, kInvThreads);
-            else __syncthreads();
-        };
+        // (warps 0-7, on CUDA cores, while MMA3 runs on the tensor cores and
+        // warps 8-15 take phase 6 as soon as MMA3 is done)
+        auto inv_sync = [&]() { ptx::named_bar_sync(kBarInv, kInvThreads); };
         if (warp < kInvThreads / 32) {
             // 5a. diagonal 16 x 16 blocks, one lane per column: T_bb = (I + A_bb)^-1
             if (warp < 2) {
@@ -854,12 +853,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 const int t = c0 + C + tid;
                 beta_n = t < T ? __ldg(a.beta + ((size_t)m * T + t) * a.H + h) : 0.f;
             }
-        }
-        if (!kSplit || warp >= kInvThreads / 32) {
+        } else {
             // ------------------------------------------------------ 6. Z = V - Y, decay S
-            // split form: warps 8-15 while warps 0-7 invert, warp w doing the
-            // units hq6 = 2 ((w - 8) / 4) and + 1 of its lane quarter; else
-            // every warp its unit hq6 = hq
+            // (warps 8-15, while warps 0-7 invert): warp w does the units hq6 =
+            // 2 ((w - 8) / 4) and + 1 of its lane quarter
             if (!ptx::mbar_wait(&bar[1], phase, kWaitBudget)) {
                 raise_error(2u);
                 ok = false;
@@ -874,8 +871,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 break;
             }
 #pragma unroll 1
-            for (int u6 = 0; u6 < (kSplit ? 2 : 1); ++u6) {
-                const int hq6 = kSplit ? 2 * ((warp - 8) >> 2) + u6 : hq;
+            for (int u6 = 0; u6 < 2; ++u6) {
+                const int hq6 = 2 * ((warp - 8) >> 2) + u6;
                 {
                     // v of tokens 16 hq6 .. + 15 at channel j from the staged chunk (0 past T)
                     float vf[16];
