@@ -155,3 +155,31 @@ def test_mixed_channel_decay_from_the_gate(K, kernel):
     o_ref, S_ref = _oracle(p)
     assert rel_err(o, o_ref) <= TOL, rel_err(o, o_ref)
     assert rel_err(S, S_ref) <= TOL
+
+
+@pytest.mark.parametrize("M,T,H", [(1, 70, 1), (3, 129, 5)])
+def test_odd_shapes(K, M, T, H):
+    """One head, and an odd head count with a ragged third chunk: the tensor
+    maps of the inputs and the output span every (stream, head) correctly."""
+    p = inputs.prefill_problem(4600 + H, M=M, T=T, H=H)
+    o, S = _run(K, p, kernel=2)
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(o, o_ref) <= TOL
+    assert rel_err(S, S_ref) <= TOL
+
+
+def test_output_rows_past_T_untouched(K):
+    """O leaves by whole 64-row tensor stores; rows past T must not be
+    written (with M > 1 they would be the next stream's). o is handed in as
+    the first T rows of a larger buffer filled with a sentinel."""
+    p = inputs.prefill_problem(4700, M=1, T=70, H=2)
+    q, k, v, alpha, beta, S = _device(p)
+    pad = torch.full((1, 128, 2, 128), 12345.0, dtype=torch.float32, device="cuda")
+    o = pad[:, :70]
+    assert o.is_contiguous()
+    K.kda_chunk_prefill_config(q, k, v, alpha, beta, S, o=o, kernel=2)
+    torch.cuda.synchronize()
+    assert K.kda_device_error() == K.KDA_OK
+    assert bool(torch.all(pad[:, 70:] == 12345.0))
+    o_ref, _ = _oracle(p)
+    assert rel_err(o.double().cpu().numpy(), o_ref) <= TOL

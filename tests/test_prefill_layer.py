@@ -115,3 +115,15 @@ def test_layer_config4_size_sampled_heads(K):
         assert rel_err(y[m, :, h], y_ref[0, :, 0]) <= TOL, ((m, h), rel_err(y[m, :, h], y_ref[0, :, 0]))
         assert rel_err(S[m, h], S_ref[0, 0]) <= TOL
         np.testing.assert_array_equal(c[m][:, :, ch], c_ref[0])
+
+
+@pytest.mark.parametrize("M,T,H", [(1, 70, 1), (3, 129, 5)])
+def test_layer_odd_shapes(K, M, T, H):
+    """One head, and an odd head count with a ragged third chunk, through the
+    5-D tensor maps over x [M][T][3][H*128]."""
+    p = inputs.prefill_layer_problem(6300 + H, M=M, T=T, H=H)
+    y, S, c = _run(K, p)
+    y_ref, S_ref, c_ref = _oracle(p)
+    assert rel_err(y, y_ref) <= TOL, rel_err(y, y_ref)
+    assert rel_err(S, S_ref) <= TOL, rel_err(S, S_ref)
+    np.testing.assert_array_equal(c, c_ref)
