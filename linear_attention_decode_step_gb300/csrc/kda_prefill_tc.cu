@@ -47,12 +47,16 @@
 // The unit lower-triangular inverse is taken on CUDA cores in 16 x 16 blocks:
 // diagonal blocks by forward substitution (one lane per column), off-diagonal
 // blocks level by level from the block recurrence T_RI = -T_RR sum_Q A_RQ T_QI.
+// Warps 0-7 take it while warps 8-15 wait for MMA3 and do phase 6 (Z = V - Y,
+// the state decay); the Kdec^T tile is built while MMA1 runs.
 //
-// Inputs arrive ahead of use: q, k, alpha of the next chunk are loaded into
-// registers once this chunk's operand tiles are built; v of the next chunk is
-// brought into shared memory by bulk copies from a side warp. O leaves through
-// shared memory with bulk copies. Every mbarrier wait is bounded; on timeout
-// the kernel sets the device error word (kda_device_error) and stops.
+// Inputs arrive ahead of use through tensor maps (cp.async.bulk.tensor): with
+// BF16 q, k the next chunk's q, k, alpha land as 128-byte-swizzled boxes in
+// the [Kd; Qd] region once MMA3 has read it (FP32 q, k are loaded into
+// registers a chunk ahead instead); v of the next chunk arrives in one tensor
+// copy; O leaves through shared memory in one tensor store. Every mbarrier
+// wait is bounded; on timeout the kernel sets the device error word
+// (kda_device_error) and stops.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -992,7 +996,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_after_sync();
 
         // ---------------------------------------------------------- 7. O out
-        // O^T (tokens 16 hq .. + 15 at value channel j) -> staging rows -> bulk copies
+        // O^T (tokens 16 hq .. + 15 at value channel j) -> staging rows -> one tensor store
         {
             float o16[16];
             umma::ld_x16(tq + TM_D3 + 64 + 16 * hq, o16);
@@ -1029,7 +1033,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
     }
 
-    // after a timeout, let a bulk copy still in flight land before the CTA's
+    // after a timeout, let a tensor copy still in flight land before the CTA's
     // shared memory goes (bounded as well)
     if (!ok && v_pending) ptx::mbar_wait(&bar[4], v_parity, kWaitBudget);
     if (!ok && qka_pending) ptx::mbar_wait(&bar[5], qka_parity, kWaitBudget);
