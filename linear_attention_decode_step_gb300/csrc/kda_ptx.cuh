@@ -83,13 +83,7 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         : "memory");
 }
 
-// Bulk copy this CTA's shared memory -> global, tracked by bulk async-groups
-// of the issuing thread. Addresses 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
+// Bulk async-groups of the issuing thread (tensor stores are tracked by them).
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
