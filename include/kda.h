@@ -223,6 +223,12 @@ typedef enum {
  * inside FP32.
  * o must not overlap any input or the state; the state must not overlap any
  * input.
+ * The tensor-core kernel moves q, k, alpha, v and o by tiled tensor copies
+ * through maps encoded on the host at each call (cuTensorMapEncodeTiled via
+ * the runtime's driver entry point): a map the driver rejects (a stride of
+ * 2^40 bytes or more, i.e. T * H * 256 * element size beyond that) returns
+ * KDA_ERR_CUDA with kda_last_cuda_error() = cudaErrorInvalidValue, and a
+ * driver without the entry point cudaErrorNotSupported, before any launch.
  */
 kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qkv_dtype,
                              const float *alpha, const float *beta, float *state, float *o,
@@ -235,7 +241,9 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qk
  * with the conv cache as left context, the forget gate from its raw input
  * (in log space), L2 norm of q and k, the chunked recurrence ("GLM-5.3 deep
  * dive" sections 8.2.3 - 8.2.5) and, optionally, the gated RMSNorm on every
- * output (8.2.4 step 7). The result equals T calls of kda_decode_step_fused.
+ * output (8.2.4 step 7). The result equals T calls of kda_decode_step_fused
+ * within the prefill's tolerance (the conv's SiLU is evaluated through a
+ * hardware tanh, relative error about 2^-11; products are TF32).
  *
  *   x           [M, T, 3, H*dk]  pre-conv q, k, v of the T tokens (x_dtype)
  *   conv_w      [3, H*dk, 4]     FP32 conv weights (as kda_conv_step)
