@@ -1,0 +1,106 @@
+"""The measurement arithmetic of bench.py, checked against counts taken from
+the tensor layouts (include/kda.h) and from the shapes of the chunked form's
+products ("GLM-5.3 deep dive", section 8.2.5), not against the closed forms
+bench.py uses. CPU only."""
+import numpy as np
+import pytest
+
+import bench
+
+H, d = 64, 128
+D = H * d
+
+
+def _nbytes(shape, elem):
+    return int(np.prod(shape)) * elem
+
+
+def test_state_bytes_per_launch():
+    for M, dt, s in [(32, "f32", 4), (32, "bf16", 2), (1, "f32", 4)]:
+        state = _nbytes((M, H, d, d), s)
+        assert bench.state_bytes_per_launch(M, dt) == 2 * state  # read + write
+
+
+@pytest.mark.parametrize("state_dtype,x_dtype", [("f32", "bf16"), ("bf16", "bf16"), ("f32", "f32")])
+def test_decode_algorithmic_bytes_from_layouts(state_dtype, x_dtype):
+    M = 32
+    s = 4 if state_dtype == "f32" else 2
+    x = 4 if x_dtype == "f32" else 2
+    total = (2 * _nbytes((M, H, d, d), s)        # state in and out
+             + _nbytes((M, 3, D), x)              # pre-conv q, k, v
+             + 2 * _nbytes((M, 3, 3, D), x)       # conv cache in and out
+             + _nbytes((M, H, d), 4)              # alpha
+             + _nbytes((M, H), 4)                 # beta
+             + _nbytes((M, H, d), 4)              # o
+             + _nbytes((3, D, 4), 4))             # conv weights, shared by the streams
+    assert bench.algorithmic_bytes_per_launch(M, state_dtype, x_dtype) == total
+
+
+def test_headline_roofline_bytes_match_the_profile_figure():
+    # the per-launch figure quoted beside the roofline in the decode profile
+    assert bench.algorithmic_bytes_per_launch(32, "f32", "bf16") == 281944064
+
+
+def test_prefill_bytes_from_layouts():
+    M, T = 4, 4096
+    total = (3 * _nbytes((M, T, H, d), 2)        # q, k, v BF16
+             + _nbytes((M, T, H, d), 4)          # alpha
+             + _nbytes((M, T, H), 4)             # beta
+             + _nbytes((M, T, H, d), 4)          # o
+             + 2 * _nbytes((M, H, d, d), 4))     # state in and out
+    assert bench.prefill_bytes(M, T, H) == total == 1916796928
+
+
+@pytest.mark.parametrize("norm", [True, False])
+def test_prefill_layer_bytes_from_layouts(norm):
+    M, T = 4, 4096
+    total = (_nbytes((M, T, 3, D), 2)            # pre-conv x BF16
+             + _nbytes((M, T, H, d), 4)          # raw gate input f
+             + _nbytes((M, T, H), 4)             # beta
+             + (_nbytes((M, T, H, d), 4) if norm else 0)  # output gate
+             + _nbytes((M, T, H, d), 4)          # y
+             + 2 * _nbytes((M, H, d, d), 4)      # state in and out
+             + 2 * _nbytes((M, 3, 3, D), 2))     # conv cache in and out
+    assert bench.prefill_layer_bytes(M, T, H, norm=norm) == total
+
+
+def test_prefill_flops_from_product_shapes():
+    """2 m n k per product, over the products of one chunk: A and P scores
+    (C x d times d x C), W and U (C x C times C x d), Kd S and Qd S (C x d
+    times d x d), the state update (d x C times C x d); ragged last chunks count
+    as whole chunks."""
+    C = 64
+    products = [(C, C, d), (C, C, d), (C, d, C), (C, d, C), (C, d, d), (C, d, d), (d, d, C)]
+    per_chunk = sum(2 * m * n * k for m, n, k in products)
+    for M, T in [(4, 4096), (2, 1000), (1, 1)]:
+        chunks = -(-T // C)
+        assert bench.prefill_flops(M, T, H) == per_chunk * M * H * chunks
+    assert abs(bench.prefill_flops(4, 4096, H) / 1e9 - 171.8) < 0.05
+
+
+def test_fp32_peak_from_unit_counts():
+    assert abs(bench.fp32_peak_tflops(2070.0) - 152 * 128 * 2 * 2.070e9 / 1e12) < 1e-9
+    assert abs(bench.fp32_peak_tflops(None) - bench.fp32_peak_tflops(2070.0)) < 1e-12
+
+
+def test_tokens_roofline_bound_switches_with_T():
+    """A multi-token call moves the state once and does 7 d^2 flops per head
+    and token: HBM-bound at small T, ALU-bound once the flops take longer."""
+    peak_hbm, mhz = 6778.3, 2070.0
+    t_hbm = 2 * 32 * H * d * d * 4 / (peak_hbm * 1e9) * 1e6
+    for T in (1, 2, 4, 8, 16, 64):
+        t_alu = 7 * d * d * 32 * H * T / (bench.fp32_peak_tflops(mhz) * 1e12) * 1e6
+        s = bench.tokens_summary(0.1, 32, T, "f32", peak_hbm, mhz)
+        assert s["bound"] == ("hbm" if t_hbm >= t_alu else "alu")
+        assert abs(s["roofline_us"] - max(t_hbm, t_alu)) < 1e-9
+        assert abs(s["frac_of_roofline"] - max(t_hbm, t_alu) / 100.0) < 1e-12
+    assert bench.tokens_summary(0.1, 32, 8, "f32", peak_hbm, mhz)["bound"] == "hbm"
+    assert bench.tokens_summary(0.1, 32, 16, "f32", peak_hbm, mhz)["bound"] == "alu"
+
+
+def test_prefill_summary_fractions():
+    s = bench.prefill_summary(1.0, 4, 4096, 6778.3, 1946.6, "k")
+    assert abs(s["gb_s"] - 1916796928 / 1e9 / 1e-3) < 1e-6
+    assert abs(s["frac_of_measured_hbm"] - s["gb_s"] / 6778.3) < 1e-12
+    assert abs(s["tf32_peak_tflop_s"] - 1946.6 / 2) < 1e-12
+    assert abs(s["tokens_per_s"] - 4 * 4096 / 1e-3) < 1e-3
