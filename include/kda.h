@@ -281,9 +281,11 @@ kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v,
  * kda_device_error — waits for `stream` (cudaStream_t as void*, NULL = legacy
  * default stream), then reads and clears the library's device error word.
  * Returns KDA_ERR_TIMEOUT if a kernel gave up a bounded device-side wait since
- * the last call (its outputs are then incomplete), KDA_ERR_CUDA if the wait or
- * the read failed, KDA_OK otherwise. The error word is shared by all streams
- * of the device.
+ * the last call (its outputs are then incomplete), KDA_ERR_ALIGNMENT if the
+ * tensor-core prefill found its dynamic shared memory not 1024-byte aligned
+ * (it then returns without computing; the swizzled tensor copies need that
+ * alignment), KDA_ERR_CUDA if the wait or the read failed, KDA_OK otherwise.
+ * The error word is shared by all streams of the device.
  */
 kda_status kda_device_error(void *stream);
 

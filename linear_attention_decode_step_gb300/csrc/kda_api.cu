@@ -332,6 +332,7 @@ kda_status kda_device_error(void *stream) {
     if (e != cudaSuccess) return cuda_status(e);
     e = kda::take_tokens_error(&code3);
     if (e != cudaSuccess) return cuda_status(e);
+    if (code2 & kda::kPrefillErrMisaligned) return KDA_ERR_ALIGNMENT;
     return (code | code2 | code3) ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 

@@ -68,6 +68,9 @@ cudaError_t launch_prefill_layer(const PrefillArgs &a, int x_dtype, cudaStream_t
 
 // Reads and clears the tensor-core prefill's device error word.
 cudaError_t take_prefill_error(unsigned int *code);
+// Bit of the prefill's error word set when its dynamic shared memory is not
+// 1024-byte aligned (every other bit marks a bounded wait that gave up).
+constexpr unsigned int kPrefillErrMisaligned = 64u;
 
 // Launches the decode kernel for the given storage types and work split.
 // Returns cudaErrorNotSupported (without launching) when no kernel is

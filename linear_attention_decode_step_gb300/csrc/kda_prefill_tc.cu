@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const int T = a.T;
     const uint32_t sbase = ptx::smem_u32(sm);
     if (sbase & 1023u) {  // the swizzled boxes need a 1024-byte aligned base
-        if (tid == 0) raise_error(64u);
+        if (tid == 0) raise_error(kPrefillErrMisaligned);
         return;
     }
 
