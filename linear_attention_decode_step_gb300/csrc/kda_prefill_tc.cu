@@ -189,6 +189,13 @@ __device__ __forceinline__ float silu(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
     return fmaf(h, t, h);
 }
+// sigmoid(x) = (1 + tanh(x / 2)) / 2 the same way, for the norm's output gate
+// (a factor on an already normalised output: its error does not accumulate)
+__device__ __forceinline__ float sigm(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
+}
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -1016,10 +1023,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 const float rn = rsqrtf(ss * (1.0f / DK) + a.norm_eps);
                 const float4 g4 = og[i];
-                o4.x = o4.x * rn * nw.x / (1.0f + __expf(-g4.x));
-                o4.y = o4.y * rn * nw.y / (1.0f + __expf(-g4.y));
-                o4.z = o4.z * rn * nw.z / (1.0f + __expf(-g4.z));
-                o4.w = o4.w * rn * nw.w / (1.0f + __expf(-g4.w));
+                o4.x = o4.x * rn * nw.x * sigm(g4.x);
+                o4.y = o4.y * rn * nw.y * sigm(g4.y);
+                o4.z = o4.z * rn * nw.z * sigm(g4.z);
+                o4.w = o4.w * rn * nw.w * sigm(g4.w);
                 *row = o4;
             }
         }
