@@ -808,45 +808,118 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 for (int r = 0; r < 16; ++r) sT[(j0 + r) * LDA + j0 + jj] = tcol[r];
             }
             inv_sync();
-            // 5b. off-diagonal blocks, level d = R - I at a time:
-            //     T_RI = -T_RR X_RI,  X_RI = sum_{Q=I}^{R-1} A_RQ T_QI
-            for (int d = 1; d < 4; ++d) {
-                const int nblk = 4 - d;
-                // unit: block I (R = I + d), row r16, four columns 4 q16 .. + 3
-                const int I = tid >> 6, r16 = (tid >> 2) & 15, q16 = tid & 3, Rb = I + d;
-                if (I < nblk) {
-                    float x4[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int Q = I; Q < Rb; ++Q) {
+            // 5b. off-diagonal blocks. The plain form, where the inverse is on the
+            //     critical path, takes the right-looking order (fewer dependent block
+            //     products); the layer form, where phase 6 is, the level order (fewer
+            //     registers).
+            if constexpr (!LAYER) {
+                // 5b. off-diagonal blocks, right-looking: X_RI = sum_{Q=I}^{R-1} A_RQ T_QI
+                //     collects each term as soon as T_QI exists (kept in the unused
+                //     upper block (I, R) of A), so every step on the critical path is one
+                //     16 x 16 block product: step 0 takes the six first terms A_RI T_II,
+                //     level L solves T_RI = -T_RR X_RI for R = I + L, step k adds
+                //     A_{R, I+k} T_{I+k, I} for R > I + k. Unit: row r16, columns 4 q16 .. + 3.
+                {
+                    const int r16 = (tid >> 2) & 15, q16 = tid & 3;
+                    // X_RI += A_{R,Q} T_{Q,I} (or =, when first)
+                    auto add_term = [&](int R, int I, int Q, int rr16, int qq16, bool first) {
+                        float x4[4] = {0.f, 0.f, 0.f, 0.f};
+                        float *xp = sA + (16 * I + rr16) * LDA + 16 * R + 4 * qq16;
+                        if (!first) {
+                            const float4 x0 = *reinterpret_cast<const float4 *>(xp);
+                            x4[0] = x0.x;
+                            x4[1] = x0.y;
+                            x4[2] = x0.z;
+                            x4[3] = x0.w;
+                        }
 #pragma unroll
                         for (int t = 0; t < 16; ++t) {
-                            const float av = sA[(16 * Rb + r16) * LDA + 16 * Q + t];
-                            const float4 tv =
-                                *reinterpret_cast<const float4 *>(sT + (16 * Q + t) * LDA + 16 * I + 4 * q16);
+                            const float av = sA[(16 * R + rr16) * LDA + 16 * Q + t];
+                            const float4 tv = *reinterpret_cast<const float4 *>(sT + (16 * Q + t) * LDA + 16 * I + 4 * qq16);
                             x4[0] = fmaf(av, tv.x, x4[0]);
                             x4[1] = fmaf(av, tv.y, x4[1]);
                             x4[2] = fmaf(av, tv.z, x4[2]);
                             x4[3] = fmaf(av, tv.w, x4[3]);
                         }
-                    }
-                    *reinterpret_cast<float4 *>(sX + (I * 16 + r16) * 16 + 4 * q16) =
-                        make_float4(x4[0], x4[1], x4[2], x4[3]);
-                }
-                inv_sync();
-                if (I < nblk) {
-                    float t4[4] = {0.f, 0.f, 0.f, 0.f};
+                        *reinterpret_cast<float4 *>(xp) = make_float4(x4[0], x4[1], x4[2], x4[3]);
+                    };
+                    // T_RI = -T_RR X_RI
+                    auto solve = [&](int R, int I) {
+                        float t4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const float tv = sT[(16 * Rb + r16) * LDA + 16 * Rb + t];
-                        const float4 xv = *reinterpret_cast<const float4 *>(sX + (I * 16 + t) * 16 + 4 * q16);
-                        t4[0] = fmaf(tv, xv.x, t4[0]);
-                        t4[1] = fmaf(tv, xv.y, t4[1]);
-                        t4[2] = fmaf(tv, xv.z, t4[2]);
-                        t4[3] = fmaf(tv, xv.w, t4[3]);
+                        for (int t = 0; t < 16; ++t) {
+                            const float tv = sT[(16 * R + r16) * LDA + 16 * R + t];
+                            const float4 xv = *reinterpret_cast<const float4 *>(sA + (16 * I + t) * LDA + 16 * R + 4 * q16);
+                            t4[0] = fmaf(tv, xv.x, t4[0]);
+                            t4[1] = fmaf(tv, xv.y, t4[1]);
+                            t4[2] = fmaf(tv, xv.z, t4[2]);
+                            t4[3] = fmaf(tv, xv.w, t4[3]);
+                        }
+                        *reinterpret_cast<float4 *>(sT + (16 * R + r16) * LDA + 16 * I + 4 * q16) =
+                            make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
+                    };
+                    // step 0: the six blocks (R, I) = (1,0) (2,0) (3,0) (2,1) (3,1) (3,2), 384 units
+                    for (int u = tid; u < 384; u += kInvThreads) {
+                        const int p = u >> 6;
+                        const int I = p < 3 ? 0 : (p < 5 ? 1 : 2), R = p < 3 ? p + 1 : (p < 5 ? p - 1 : 3);
+                        add_term(R, I, I, (u >> 2) & 15, u & 3, true);
                     }
-                    *reinterpret_cast<float4 *>(sT + (16 * Rb + r16) * LDA + 16 * I + 4 * q16) =
-                        make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
+                    inv_sync();
+                    if (tid < 192) solve((tid >> 6) + 1, tid >> 6);                       // T_10, T_21, T_32
+                    inv_sync();
+                    if (tid < 192) {                                                      // (2,0) (3,0) (3,1) += A T_{I+1,I}
+                        const int p = tid >> 6, I = p < 2 ? 0 : 1, R = p == 0 ? 2 : 3;
+                        add_term(R, I, I + 1, r16, q16, false);
+                    }
+                    inv_sync();
+                    if (tid < 128) solve((tid >> 6) + 2, tid >> 6);                       // T_20, T_31
+                    inv_sync();
+                    if (tid < 64) add_term(3, 0, 2, r16, q16, false);                     // (3,0) += A_32 T_20
+                    inv_sync();
+                    if (tid < 64) solve(3, 0);                                            // T_30
+                    inv_sync();
                 }
-                inv_sync();
+            } else {
+                // 5b. off-diagonal blocks, level d = R - I at a time:
+                //     T_RI = -T_RR X_RI,  X_RI = sum_{Q=I}^{R-1} A_RQ T_QI
+                for (int d = 1; d < 4; ++d) {
+                    const int nblk = 4 - d;
+                    // unit: block I (R = I + d), row r16, four columns 4 q16 .. + 3
+                    const int I = tid >> 6, r16 = (tid >> 2) & 15, q16 = tid & 3, Rb = I + d;
+                    if (I < nblk) {
+                        float x4[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int Q = I; Q < Rb; ++Q) {
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) {
+                                const float av = sA[(16 * Rb + r16) * LDA + 16 * Q + t];
+                                const float4 tv =
+                                    *reinterpret_cast<const float4 *>(sT + (16 * Q + t) * LDA + 16 * I + 4 * q16);
+                                x4[0] = fmaf(av, tv.x, x4[0]);
+                                x4[1] = fmaf(av, tv.y, x4[1]);
+                                x4[2] = fmaf(av, tv.z, x4[2]);
+                                x4[3] = fmaf(av, tv.w, x4[3]);
+                            }
+                        }
+                        *reinterpret_cast<float4 *>(sX + (I * 16 + r16) * 16 + 4 * q16) =
+                            make_float4(x4[0], x4[1], x4[2], x4[3]);
+                    }
+                    inv_sync();
+                    if (I < nblk) {
+                        float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float tv = sT[(16 * Rb + r16) * LDA + 16 * Rb + t];
+                            const float4 xv = *reinterpret_cast<const float4 *>(sX + (I * 16 + t) * 16 + 4 * q16);
+                            t4[0] = fmaf(tv, xv.x, t4[0]);
+                            t4[1] = fmaf(tv, xv.y, t4[1]);
+                            t4[2] = fmaf(tv, xv.z, t4[2]);
+                            t4[3] = fmaf(tv, xv.w, t4[3]);
+                        }
+                        *reinterpret_cast<float4 *>(sT + (16 * Rb + r16) * LDA + 16 * I + 4 * q16) =
+                            make_float4(-t4[0], -t4[1], -t4[2], -t4[3]);
+                    }
+                    inv_sync();
+                }
             }
             // 5c. M[r][i] = T[r][i] beta_i (lower with diagonal) into the operand tile
 #pragma unroll
