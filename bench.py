@@ -163,12 +163,14 @@ class DecodeStack:
     """L independent KDA layers resident on one GPU, with pinned host
     mirrors of the per-step inputs and outputs for the end-to-end leg."""
 
-    def __init__(self, torch, kda, inputs, M, L, state_dtype, x_dtype, device, seed_cfg=3,
+    def __init__(self, torch, kda, inputs, M, L, state_dtype, x_dtype, device, seed_space=None,
                  kernel=0, columns=0, threads=0, replicate=False, rank=0):
         """replicate=True draws one layer's inputs and copies them into every
         layer's buffers (used by the sweep, where only timing matters)."""
         self.torch, self.kda, self.M, self.L = torch, kda, M, L
         self.state_dtype, self.x_dtype = state_dtype, x_dtype
+        if seed_space is None:
+            seed_space = inputs.SEED_DECODE_STACK
         D = H * DH
         xt = torch.bfloat16 if x_dtype == "bf16" else torch.float32
         st = torch.bfloat16 if state_dtype == "bf16" else torch.float32
@@ -184,7 +186,7 @@ class DecodeStack:
         self.host0 = None
         for l in range(L):
             if l == 0 or not replicate:
-                inp = inputs.decode_layer(replicas.rank_layer_seed(seed_cfg, l, rank), M=M, T=1)
+                inp = inputs.decode_layer(replicas.rank_layer_seed(seed_space, l, rank), M=M, T=1)
             if l == 0:
                 self.host0 = inp
             if x_dtype == "bf16":
@@ -444,7 +446,7 @@ def prefill_flops(M, T, H, chunk=64):
 def time_prefill(torch, kda, inputs, M, T, K, W, kernel=0):
     """K chunked prefills of one (M, T, 64-head) problem resident on the GPU,
     timed with CUDA events around the whole run (state updated in place)."""
-    p = inputs.prefill_problem(inputs.layer_seed(4, 0), M=M, T=T, H=H)
+    p = inputs.prefill_problem(inputs.layer_seed(inputs.SEED_PREFILL_M4_T4096, 0), M=M, T=T, H=H)
     dev = torch.device("cuda")
     bf = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
     q, k, v = bf(p["q_bits"]), bf(p["k_bits"]), bf(p["v_bits"])
@@ -472,7 +474,7 @@ def time_prefill_layer(torch, kda, inputs, M, T, K, W, norm=True):
     """K calls of kda_prefill_layer (conv + gate + chunked recurrence + gated
     RMSNorm) on one (M, T, 64-head) prompt resident on the GPU; state and
     cache updated in place. Returns ms per call."""
-    p = inputs.prefill_layer_problem(inputs.layer_seed(4, 2), M=M, T=T, H=H)
+    p = inputs.prefill_layer_problem(inputs.layer_seed(inputs.SEED_PREFILL_M4_T4096, 2), M=M, T=T, H=H)
     dev = torch.device("cuda")
     bf = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
     x, cache = bf(p["x_bits"]), bf(p["cache_bits"])
@@ -538,7 +540,7 @@ def time_tokens(torch, kda, inputs, M, T, state_dtype, K, W):
     """K multi-token decode calls (T tokens each) of one layer at M streams x
     64 heads, alternating between two state buffers (together larger than L2).
     Returns ms per call."""
-    inp = inputs.decode_layer(inputs.layer_seed(5, T), M=M, H=H, T=T)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_TOKENS, T), M=M, H=H, T=T)
     tok = inputs.stack_tokens(inp)
     dev = torch.device("cuda")
     bf = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -658,7 +660,9 @@ class OraclePool:
 
 
 def inputs_seed(l: int) -> int:
-    return 1000 * 3 + l  # the decode stack's per-layer seed (config 3, layer l)
+    """Seed of layer l of the 34-layer decode stack."""
+    from linear_attention_decode_step_gb300 import inputs
+    return inputs.layer_seed(inputs.SEED_DECODE_STACK, l)
 
 
 def oracle_all_cores_sample(budget_s: float):

@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, overlapping outputs */
-    KDA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. dk != 128) */
+    KDA_ERR_UNSUPPORTED = 2, /* valid request this library does not implement (e.g. dk != 128) */
     KDA_ERR_ALIGNMENT = 3,   /* a buffer pointer is not 16-byte aligned */
     KDA_ERR_CUDA = 4,        /* a CUDA runtime call failed; see kda_last_cuda_error() */
     KDA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up */

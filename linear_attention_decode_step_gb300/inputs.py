@@ -34,6 +34,12 @@ __all__ = [
     "decode_layer",
     "prefill_problem",
     "layer_seed",
+    "SEED_DECODE_M1_T16",
+    "SEED_DECODE_M8",
+    "SEED_DECODE_M32_BF16",
+    "SEED_DECODE_STACK",
+    "SEED_PREFILL_M4_T4096",
+    "SEED_DECODE_TOKENS",
     "gate_norm_inputs",
     "stack_tokens",
     "prefill_layer_problem",
@@ -65,9 +71,18 @@ def _sigmoid32(z: np.ndarray) -> np.ndarray:
     return (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
 
 
-def layer_seed(config: int, layer: int) -> int:
-    """Per-layer seed: 1000 * config + layer."""
-    return 1000 * config + layer
+# Seed spaces, 1000 seeds each, one per synthetic workload:
+SEED_DECODE_M1_T16 = 0      # one layer, M = 1, 16 consecutive FP32-state steps
+SEED_DECODE_M8 = 1          # one layer, M = 8, one FP32-state step
+SEED_DECODE_M32_BF16 = 2    # one layer, M = 32, one BF16-state step
+SEED_DECODE_STACK = 3       # the 34-layer decode stack (seed = layer index)
+SEED_PREFILL_M4_T4096 = 4   # prefill, M = 4 streams x T = 4096 tokens
+SEED_DECODE_TOKENS = 5      # multi-token decode (seed = token count)
+
+
+def layer_seed(space: int, layer: int) -> int:
+    """Per-layer seed: 1000 * space + layer, space one of the SEED_* above."""
+    return 1000 * space + layer
 
 
 def decode_layer(seed: int, M: int, H: int = 64, d: int = 128, T: int = 1,

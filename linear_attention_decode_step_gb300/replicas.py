@@ -14,9 +14,9 @@ from . import inputs
 RANK_SEED_STRIDE = 100_000
 
 
-def rank_layer_seed(config: int, layer: int, rank: int) -> int:
+def rank_layer_seed(space: int, layer: int, rank: int) -> int:
     """Seed of `layer` on `rank`: the single-GPU seed, offset per rank."""
-    return inputs.layer_seed(config, layer) + RANK_SEED_STRIDE * rank
+    return inputs.layer_seed(space, layer) + RANK_SEED_STRIDE * rank
 
 
 def max_over_ranks(values, dist=None, device=None):

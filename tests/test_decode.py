@@ -62,26 +62,26 @@ def _compare(dl, outs, ref_outs, S_ref, cache_ref, tol):
     np.testing.assert_array_equal(to_f64(dl.cache), cache_ref)
 
 
-def test_config0_fp32_sixteen_steps(K):
+def test_M1_fp32_sixteen_steps(K):
     """M=1, H=64, 128x128, FP32 state, 16 consecutive steps from seed."""
-    inp = inputs.decode_layer(inputs.layer_seed(0, 0), M=1, T=16)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_M1_T16, 0), M=1, T=16)
     dl = DeviceLayer(inp, "f32")
     outs = _run(K, dl, 16)
     ref, S, cache = oracle_layer(inp)
     _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
 
 
-def test_config1_fp32_M8(K):
-    inp = inputs.decode_layer(inputs.layer_seed(1, 0), M=8, T=1)
+def test_M8_fp32_one_step(K):
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_M8, 0), M=8, T=1)
     dl = DeviceLayer(inp, "f32")
     outs = _run(K, dl, 1)
     ref, S, cache = oracle_layer(inp)
     _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
 
 
-def test_config2_bf16_M32(K):
+def test_M32_bf16_one_step(K):
     """M=32, BF16 state storage, FP32 arithmetic; S0 identical to the FP32 run."""
-    inp = inputs.decode_layer(inputs.layer_seed(2, 0), M=32, T=1)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_M32_BF16, 0), M=32, T=1)
     dl = DeviceLayer(inp, "bf16")
     outs = _run(K, dl, 1)
     ref, S, cache = oracle_layer(inp)
@@ -96,7 +96,7 @@ def test_config2_bf16_M32(K):
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
 def test_M32_one_step(K, state_dtype):
     """The benchmarked workload: M=32, one step, fused conv."""
-    inp = inputs.decode_layer(inputs.layer_seed(3, 32), M=32, T=1)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, 32), M=32, T=1)
     dl = DeviceLayer(inp, state_dtype)
     outs = _run(K, dl, 1)
     ref, S, cache = oracle_layer(inp)
@@ -112,7 +112,7 @@ TILES = [(16, 64), (32, 64), (32, 128), (64, 128), (64, 256), (128, 256)]
 def test_each_kernel_M32(K, kernel, state_dtype, x_dtype):
     """Both decode kernels at M=32 (2048 heads: many heads per CTA for the
     streaming kernel, so every ring stage is reused), three steps."""
-    inp = inputs.decode_layer(inputs.layer_seed(3, 100), M=32, T=3)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, 100), M=32, T=3)
     dl = DeviceLayer(inp, state_dtype, x_dtype)
     kern = K.KDA_DECODE_CLUSTER if kernel == "cluster" else K.KDA_DECODE_STREAM
     outs = _run(K, dl, 3, kernel=kern) if kernel == "stream" else _run(K, dl, 3, tile=(32, 128))
@@ -126,7 +126,7 @@ def test_stream_kernel_ring_configs(K, groups, prefetch, state_dtype):
     """One or two consumer groups on a ring of 3 (FP32) or 5 (BF16) stages,
     with and without L2 prefetch: 2048 heads over the SMs reuse every stage
     many times, so both mbarrier parities and the refill order are exercised."""
-    inp = inputs.decode_layer(inputs.layer_seed(3, 200 + groups), M=32, T=2)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, 200 + groups), M=32, T=2)
     dl = DeviceLayer(inp, state_dtype)
     outs = _run(K, dl, 2, kernel=K.KDA_DECODE_STREAM, stream_cfg=(prefetch, groups))
     ref, S, cache = oracle_layer(inp)
@@ -165,7 +165,7 @@ def test_odd_sizes_and_scale(K):
 
 
 def test_max_streams_M64(K):
-    inp = inputs.decode_layer(inputs.layer_seed(3, 64), M=64, T=1)
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, 64), M=64, T=1)
     dl = DeviceLayer(inp, "f32")
     outs = _run(K, dl, 1)
     ref, S, cache = oracle_layer(inp)
@@ -217,7 +217,7 @@ def test_34_layer_stack_under_cuda_graph(K, state_dtype):
     """34 independent layers, M=8, one token, launched as one captured CUDA
     graph (the bench's launch configuration); every layer checked."""
     L, M = 34, 8
-    layers = [DeviceLayer(inputs.decode_layer(inputs.layer_seed(3, l), M=M, T=1), state_dtype)
+    layers = [DeviceLayer(inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, l), M=M, T=1), state_dtype)
               for l in range(L)]
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):

@@ -126,12 +126,12 @@ def test_identity_steps_read_state(K, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_config4_full_size_sampled_heads(K, kernel):
+def test_M4_T4096_sampled_heads(K, kernel):
     """M=4 streams, T=4096 tokens, 64 heads, chunk 64, BF16 q/k/v, FP32
     state: the whole problem runs on the GPU; six (stream, head) pairs are
     checked against 4096 sequential oracle steps each (every output of those
     heads and their final state)."""
-    p = inputs.prefill_problem(inputs.layer_seed(4, 0), M=4, T=4096, H=64)
+    p = inputs.prefill_problem(inputs.layer_seed(inputs.SEED_PREFILL_M4_T4096, 0), M=4, T=4096, H=64)
     o, S = _run(K, p, kernel=kernel)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
     heads = [(0, 0), (1, 17), (2, 33), (3, 63), (0, 48), (3, 5)]

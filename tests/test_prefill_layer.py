@@ -95,10 +95,10 @@ def test_layer_matches_decode_steps_on_device(K):
     np.testing.assert_array_equal(c, to_f64(cache))
 
 
-def test_layer_config4_size_sampled_heads(K):
+def test_layer_M4_T4096_sampled_heads(K):
     """M=4 streams, T=4096 tokens, 64 heads (the prefill workload) as a whole
     layer: three (stream, head) pairs checked against 4096 oracle steps."""
-    p = inputs.prefill_layer_problem(inputs.layer_seed(4, 1), M=4, T=4096, H=64)
+    p = inputs.prefill_layer_problem(inputs.layer_seed(inputs.SEED_PREFILL_M4_T4096, 1), M=4, T=4096, H=64)
     y, S, c = _run(K, p)
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(S))
     for (m, h) in [(0, 0), (2, 31), (3, 63)]:

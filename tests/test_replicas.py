@@ -9,7 +9,7 @@ torch = pytest.importorskip("torch")
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
-from linear_attention_decode_step_gb300 import replicas
+from linear_attention_decode_step_gb300 import inputs, replicas
 
 
 def _free_port():
@@ -26,7 +26,7 @@ def _rank_main(rank, world, port, out):
         local = [1.0 + rank, 10.0 - rank]
         dist.barrier()
         got = replicas.max_over_ranks(local, dist)
-        seeds = [replicas.rank_layer_seed(3, l, rank) for l in range(34)]
+        seeds = [replicas.rank_layer_seed(inputs.SEED_DECODE_STACK, l, rank) for l in range(34)]
         allseeds = [None] * world
         dist.all_gather_object(allseeds, seeds)
         out[rank] = (got, allseeds)
@@ -49,6 +49,6 @@ def test_two_gloo_ranks_max_and_distinct_seeds():
 
 def test_single_process_passthrough_and_aggregate():
     assert replicas.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
-    assert replicas.rank_layer_seed(3, 5, 0) == 3005
+    assert replicas.rank_layer_seed(inputs.SEED_DECODE_STACK, 5, 0) == 3005
     # weak scaling: 2 ranks x 1 GB in 0.5 s (slowest rank) -> 4 GB/s
     assert replicas.job_throughput(1e9, 2, 0.5) == 4e9
