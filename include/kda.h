@@ -33,7 +33,8 @@
  *   - No exceptions cross this boundary. There is no CPU fallback: every step
  *     of the computation runs in this library's kernels.
  *   - The entry points are thread-safe; they keep no mutable global state
- *     other than the per-thread last CUDA error.
+ *     other than the per-thread last CUDA error and, on each device, the
+ *     device error word that bounded waits set (see kda_device_error).
  */
 #ifndef KDA_GB300_H
 #define KDA_GB300_H

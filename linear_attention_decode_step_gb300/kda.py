@@ -27,7 +27,7 @@ __all__ = [
     "KdaError", "lib", "library_path", "header_functions",
     "kda_status_string", "kda_last_cuda_error", "kda_version",
     "kda_conv_step", "kda_decode_step", "kda_decode_step_config", "kda_device_error",
-    "kda_decode_step_fused",
+    "kda_decode_step_fused", "kda_decode_tokens", "kda_prefill_layer",
 ]
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED = 0, 1, 2

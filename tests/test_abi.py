@@ -29,8 +29,11 @@ def test_header_symbols_exported(K):
                          capture_output=True, text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     assert set(names) <= exported
-    # every declared function has a binding signature
+    # every declared function has a binding signature and a public wrapper
     assert set(names) <= set(K._SIGNATURES)
+    assert set(names) <= set(K.__all__)
+    for n in names:
+        assert callable(getattr(K, n)), n
 
 
 def test_status_strings(K):
