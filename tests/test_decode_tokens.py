@@ -39,10 +39,16 @@ def _device(inp, tok, state_dtype, x_dtype):
             torch.from_numpy(tok["alpha"]).to(dev), torch.from_numpy(tok["beta"]).to(dev), S)
 
 
-def _check(K, M, H, T, state_dtype="f32", x_dtype="bf16", scale=1.0, seed=0):
+def _check(K, M, H, T, state_dtype="f32", x_dtype="bf16", scale=1.0, seed=0, edit=None):
+    """Runs T tokens through kda_decode_tokens and checks them against the
+    oracle; `edit(inp, tok)` may overwrite the drawn inputs first. Returns the
+    device outputs (o, final state, initial state)."""
     inp = inputs.decode_layer(8000 + seed, M=M, H=H, T=T)
     tok = inputs.stack_tokens(inp)
+    if edit is not None:
+        edit(inp, tok)
     x, w, cache, alpha, beta, S = _device(inp, tok, state_dtype, x_dtype)
+    S_before = S.clone()
     o = K.kda_decode_tokens(x, w, cache, alpha, beta, S, scale=scale)
     torch.cuda.synchronize()
     assert K.kda_device_error() == K.KDA_OK
@@ -54,6 +60,7 @@ def _check(K, M, H, T, state_dtype="f32", x_dtype="bf16", scale=1.0, seed=0):
         assert rel_err(o[:, t], o_ref[:, t]) <= tol, (t, rel_err(o[:, t], o_ref[:, t]))
     assert rel_err(to_f64(S), S_ref) <= tol, rel_err(to_f64(S), S_ref)
     np.testing.assert_array_equal(to_f64(cache), c_ref)
+    return o, S, S_before
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 8, 17])
@@ -81,6 +88,30 @@ def test_tokens_single_stream_single_head(K):
 def test_tokens_long_run(K):
     """64 tokens in one call (the longest draft the page's MTP use suggests)."""
     _check(K, 2, 4, 64, seed=60)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_tokens_identity_leaves_state(K, state_dtype):
+    """alpha = 1, beta = 0 for every token: the state comes back bit for bit
+    (the fade multiplies by exactly 1, the correction adds exactly 0) and each
+    o_t = S0^T q_t."""
+    def identity(inp, tok):
+        tok["alpha"] = np.ones_like(tok["alpha"])
+        tok["beta"] = np.zeros_like(tok["beta"])
+    _, S, S_before = _check(K, 3, 6, 5, state_dtype, seed=70, edit=identity)
+    assert torch.equal(S, S_before)
+
+
+def test_tokens_zero_input_degenerate(K):
+    """All-zero pre-conv inputs and cache: q = k = v = 0 after the conv, so
+    every o_t is exactly 0 and the state is only faded, token by token."""
+    def zero(inp, tok):
+        for n in ("x_bits", "x_f32"):
+            tok[n] = np.zeros_like(tok[n])
+        for n in ("cache_bits", "cache_f32"):
+            inp[n] = np.zeros_like(inp[n])
+    o, _, _ = _check(K, 2, 4, 6, seed=80, edit=zero)
+    assert np.all(o == 0.0)
 
 
 def test_one_token_matches_decode_step(K):

@@ -126,6 +126,21 @@ def test_identity_steps_read_state(K, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+def test_zero_query_and_key_only_decay(K, kernel):
+    """q = k = 0 (normalised to 0 through the eps): nothing is written or
+    read, so every o_t is exactly 0 and the state is S0 scaled row by row by
+    the product of the alphas; across chunk boundaries and a ragged tail."""
+    p = inputs.prefill_problem(4800, M=2, T=150, H=3, alpha_mean=4.0)
+    for n in ("q", "k"):
+        p[n] = np.zeros_like(p[n])
+        p[n + "_bits"] = np.zeros_like(p[n + "_bits"])
+    o, S = _run(K, p, kernel=kernel)
+    assert np.all(o == 0.0)
+    o_ref, S_ref = _oracle(p)
+    assert rel_err(S, S_ref) <= TOL
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_M4_T4096_sampled_heads(K, kernel):
     """M=4 streams, T=4096 tokens, 64 heads, chunk 64, BF16 q/k/v, FP32
     state: the whole problem runs on the GPU; six (stream, head) pairs are

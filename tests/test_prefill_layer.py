@@ -73,6 +73,20 @@ def test_layer_without_norm_and_scaled(K, x_dtype):
     np.testing.assert_array_equal(c, c_ref)
 
 
+def test_layer_zero_input_only_decays(K):
+    """All-zero pre-conv inputs and cache: q = k = v = 0 after the conv, so
+    every output (after the gated norm too) is exactly 0, the state is only
+    faded by the gate's decay, and the cache stays zero."""
+    p = inputs.prefill_layer_problem(6300, M=2, T=100, H=3)
+    for n in ("x_bits", "x_f32", "cache_bits", "cache_f32"):
+        p[n] = np.zeros_like(p[n])
+    y, S, c = _run(K, p)
+    assert np.all(y == 0.0)
+    y_ref, S_ref, c_ref = _oracle(p)
+    assert rel_err(S, S_ref) <= TOL
+    np.testing.assert_array_equal(c, c_ref)
+
+
 def test_layer_matches_decode_steps_on_device(K):
     """Prefill of 9 tokens equals 9 fused decode steps on the GPU (same
     inputs, state and cache carried)."""
