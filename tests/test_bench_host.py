@@ -104,3 +104,32 @@ def test_prefill_summary_fractions():
     assert abs(s["frac_of_measured_hbm"] - s["gb_s"] / 6778.3) < 1e-12
     assert abs(s["tf32_peak_tflop_s"] - 1946.6 / 2) < 1e-12
     assert abs(s["tokens_per_s"] - 4 * 4096 / 1e-3) < 1e-3
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores) prints
+    one JSON line with the metric, unit and direction of this library's arm,
+    its own e2e object (no host-device bytes) and a cpu_baseline that names
+    the oracle and the cores it used. Runs on the CPU in a few seconds."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3"],
+                         capture_output=True, text=True, check=True, timeout=600, cwd=root)
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, out.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["n_gpus"] == 1
+    assert line["steps"] == 1 and line["warmup"] == 3
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert line["config"]["M"] == 32 and line["config"]["layers"] == 34
