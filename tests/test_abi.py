@@ -182,3 +182,21 @@ def _layer_call(K, **over):
 ])
 def test_layer_rejects(K, over, status):
     assert _layer_call(K, **over) == status
+
+
+def test_plain_c_caller(K, tmp_path):
+    """The header compiles as strict C99 (gcc -pedantic -Werror, no C++ or
+    CUDA headers) and a C program linked with the library gets the documented
+    statuses from the host-side checks (tests/c/abi_caller.c)."""
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(K.library_path())
+    exe = tmp_path / "abi_caller"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(root, "include"),
+                    os.path.join(root, "tests", "c", "abi_caller.c"),
+                    "-L", libdir, "-lkda_gb300", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "abi_caller: ok"
