@@ -81,7 +81,8 @@ int kda_version(void);
  *                            Updated in place to (tap1, tap2, x).
  *   y           [M, 3, D]    FP32 output: SiLU(w . [cache, x])
  *   M >= 1 streams, D >= 1 channels per tensor.
- * y must not overlap x, conv_w or conv_cache.
+ * y and conv_cache (the buffers the call writes) must not overlap each other,
+ * x or conv_w; an overlap returns KDA_ERR_INVALID_ARG.
  */
 kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w,
                          void *conv_cache, int cache_dtype, float *y,
@@ -104,7 +105,8 @@ kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w,
  *   scale       multiplies the readout (1.0 reproduces Eq. 1)
  *   o           [M, H, dv]   FP32 output
  *   dk = dv = 128 (other sizes return KDA_ERR_UNSUPPORTED); 1 <= M, H <= 65535.
- * o must not overlap state, conv_cache or x; state must not overlap conv_cache.
+ * The buffers the call writes (o, state, conv_cache) must not overlap each
+ * other or any input; an overlap returns KDA_ERR_INVALID_ARG.
  */
 kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w,
                            void *conv_cache, int cache_dtype,
@@ -127,8 +129,9 @@ kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w,
  *   norm_eps                RMSNorm eps (1e-5 in GLM-5.3-Flash)
  *   y           [M, H, dv]  FP32 output: o, or with out_gate
  *                           o / sqrt(mean(o^2) + norm_eps) * norm_weight * sigmoid(out_gate)
- * All other arguments, layouts and checks as kda_decode_step; y must not
- * overlap any input or the state.
+ * All other arguments, layouts and checks as kda_decode_step; the buffers the
+ * call writes (y, state, conv_cache) must not overlap each other or any
+ * input, the gate and norm inputs included.
  */
 kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w,
                                  void *conv_cache, int cache_dtype,

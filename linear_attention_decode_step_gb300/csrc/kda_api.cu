@@ -33,6 +33,25 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+// A buffer as the byte range a call touches (p may be null for an absent
+// optional input).
+struct Span {
+    const void *p;
+    size_t n;
+};
+
+// Every buffer a call writes is disjoint from every other one it writes and
+// from every buffer it reads.
+bool writes_disjoint(const Span *outs, int n_out, const Span *ins, int n_in) {
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return false;
+        for (int j = 0; j < n_in; ++j)
+            if (ins[j].p && overlap(outs[i].p, outs[i].n, ins[j].p, ins[j].n)) return false;
+    }
+    return true;
+}
+
 kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *conv_cache,
                         int cache_dtype, const float *alpha, const float *beta, void *state,
                         int state_dtype, float *o, int M, int H, int dk, int dv, int T = 1) {
@@ -48,13 +67,14 @@ kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *c
         !aligned16(beta) || !aligned16(state) || !aligned16(o))
         return KDA_ERR_ALIGNMENT;
     const size_t D = (size_t)H * dk;
-    const size_t n_state = (size_t)M * H * dk * dv * dtype_bytes(state_dtype);
-    const size_t n_o = (size_t)M * T * H * dv * sizeof(float);
-    const size_t n_cache = (size_t)M * 9 * D * dtype_bytes(cache_dtype);
-    const size_t n_x = (size_t)M * T * 3 * D * dtype_bytes(x_dtype);
-    if (overlap(o, n_o, state, n_state) || overlap(o, n_o, conv_cache, n_cache) ||
-        overlap(o, n_o, x, n_x) || overlap(state, n_state, conv_cache, n_cache))
-        return KDA_ERR_INVALID_ARG;
+    const Span outs[3] = {{o, (size_t)M * T * H * dv * sizeof(float)},
+                          {state, (size_t)M * H * dk * dv * dtype_bytes(state_dtype)},
+                          {conv_cache, (size_t)M * 9 * D * dtype_bytes(cache_dtype)}};
+    const Span ins[4] = {{x, (size_t)M * T * 3 * D * dtype_bytes(x_dtype)},
+                         {conv_w, (size_t)3 * D * 4 * sizeof(float)},
+                         {alpha, (size_t)M * T * H * dk * sizeof(float)},
+                         {beta, (size_t)M * T * H * sizeof(float)}};
+    if (!writes_disjoint(outs, 3, ins, 4)) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
 
@@ -72,14 +92,10 @@ kda_status check_prefill(const void *q, const void *k, const void *v, int qkv_dt
         return KDA_ERR_ALIGNMENT;
     const size_t tok = (size_t)M * T * H;
     const size_t n_qkv = tok * dk * dtype_bytes(qkv_dtype);
-    const size_t n_a = tok * dk * 4, n_b = tok * 4, n_o = tok * dv * 4;
-    const size_t n_s = (size_t)M * H * dk * dv * 4;
-    const void *ins[5] = {q, k, v, alpha, beta};
-    const size_t ns[5] = {n_qkv, n_qkv, n_qkv, n_a, n_b};
-    for (int i = 0; i < 5; ++i)
-        if (overlap(o, n_o, ins[i], ns[i]) || overlap(state, n_s, ins[i], ns[i]))
-            return KDA_ERR_INVALID_ARG;
-    if (overlap(o, n_o, state, n_s)) return KDA_ERR_INVALID_ARG;
+    const Span outs[2] = {{o, tok * dv * 4}, {state, (size_t)M * H * dk * dv * 4}};
+    const Span ins[5] = {{q, n_qkv}, {k, n_qkv}, {v, n_qkv}, {alpha, tok * dk * 4},
+                         {beta, tok * 4}};
+    if (!writes_disjoint(outs, 2, ins, 5)) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
 
@@ -111,12 +127,11 @@ kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w, void *
     if (cache_dtype != x_dtype) return KDA_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_cache) || !aligned16(y))
         return KDA_ERR_ALIGNMENT;
-    const size_t n_y = (size_t)M * 3 * D * sizeof(float);
     const size_t b = dtype_bytes(x_dtype);
-    if (overlap(y, n_y, x, (size_t)M * 3 * D * b) ||
-        overlap(y, n_y, conv_cache, (size_t)M * 9 * D * b) ||
-        overlap(y, n_y, conv_w, (size_t)3 * D * 4 * sizeof(float)))
-        return KDA_ERR_INVALID_ARG;
+    const Span outs[2] = {{y, (size_t)M * 3 * D * sizeof(float)},
+                          {conv_cache, (size_t)M * 9 * D * b}};
+    const Span ins[2] = {{x, (size_t)M * 3 * D * b}, {conv_w, (size_t)3 * D * 4 * sizeof(float)}};
+    if (!writes_disjoint(outs, 2, ins, 2)) return KDA_ERR_INVALID_ARG;
     return cuda_status(kda::launch_conv(x, x_dtype, conv_w, conv_cache, y, M, D,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -227,19 +242,18 @@ kda_status kda_prefill_layer(const void *x, int x_dtype, const float *conv_w, vo
         (norm_weight && !aligned16(norm_weight)))
         return KDA_ERR_ALIGNMENT;
     const size_t D = (size_t)H * dk, tok = (size_t)M * T * H;
-    const size_t n_x = (size_t)M * T * 3 * D * dtype_bytes(x_dtype);
-    const size_t n_c = (size_t)M * 9 * D * dtype_bytes(cache_dtype);
-    const size_t n_f = tok * dk * 4, n_b = tok * 4, n_y = tok * dv * 4;
-    const size_t n_s = (size_t)M * H * dk * dv * 4;
-    const void *ins[4] = {x, gate_f, beta, out_gate};
-    const size_t ns[4] = {n_x, n_f, n_b, out_gate ? n_y : 0};
-    for (int i = 0; i < 4; ++i)
-        if (ins[i] && (overlap(y, n_y, ins[i], ns[i]) || overlap(state, n_s, ins[i], ns[i]) ||
-                       overlap(conv_cache, n_c, ins[i], ns[i])))
-            return KDA_ERR_INVALID_ARG;
-    if (overlap(y, n_y, state, n_s) || overlap(y, n_y, conv_cache, n_c) ||
-        overlap(state, n_s, conv_cache, n_c))
-        return KDA_ERR_INVALID_ARG;
+    const Span outs[3] = {{y, tok * dv * 4},
+                          {state, (size_t)M * H * dk * dv * 4},
+                          {conv_cache, (size_t)M * 9 * D * dtype_bytes(cache_dtype)}};
+    const Span ins[8] = {{x, (size_t)M * T * 3 * D * dtype_bytes(x_dtype)},
+                         {conv_w, 3 * D * 4 * sizeof(float)},
+                         {gate_f, tok * dk * 4},
+                         {A_log, (size_t)H * sizeof(float)},
+                         {dt_bias, D * sizeof(float)},
+                         {beta, tok * 4},
+                         {out_gate, tok * dv * 4},
+                         {norm_weight, (size_t)dv * sizeof(float)}};
+    if (!writes_disjoint(outs, 3, ins, 8)) return KDA_ERR_INVALID_ARG;
     kda::PrefillArgs a = {};
     a.q = x;
     a.alpha = gate_f;
@@ -274,10 +288,16 @@ kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w
     if (!aligned16(A_log) || !aligned16(dt_bias) || (out_gate && !aligned16(out_gate)) ||
         (norm_weight && !aligned16(norm_weight)))
         return KDA_ERR_ALIGNMENT;
-    const size_t n_y = (size_t)M * H * dv * sizeof(float);
-    if (overlap(y, n_y, gate_f, (size_t)M * H * dk * sizeof(float)) ||
-        (out_gate && overlap(y, n_y, out_gate, n_y)))
-        return KDA_ERR_INVALID_ARG;
+    // beyond check_decode: the written buffers against the gate and norm inputs
+    const size_t D = (size_t)H * dk;
+    const Span outs[3] = {{y, (size_t)M * H * dv * sizeof(float)},
+                          {state, (size_t)M * H * dk * dv * dtype_bytes(state_dtype)},
+                          {conv_cache, (size_t)M * 9 * D * dtype_bytes(cache_dtype)}};
+    const Span ins[4] = {{A_log, (size_t)H * sizeof(float)},
+                         {dt_bias, D * sizeof(float)},
+                         {out_gate, (size_t)M * H * dv * sizeof(float)},
+                         {norm_weight, (size_t)dv * sizeof(float)}};
+    if (!writes_disjoint(outs, 3, ins, 4)) return KDA_ERR_INVALID_ARG;
     kda::DecodeArgs a = {};
     a.x = x;
     a.conv_w = conv_w;

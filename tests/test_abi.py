@@ -78,6 +78,10 @@ def test_decode_misaligned(K, field):
     (dict(cd=0), 2),                       # cache dtype must equal x dtype
     (dict(o=BASE + 5 * GAP + 1024), 1),    # o inside the state buffer
     (dict(cache=BASE + 5 * GAP), 1),       # cache aliases the state
+    (dict(o=BASE + 3 * GAP + 64), 1),      # o inside alpha
+    (dict(o=BASE + 4 * GAP + 16), 1),      # o inside beta
+    (dict(state=BASE + 16), 1),            # state overlaps x
+    (dict(cache=BASE + GAP + 32), 1),      # cache inside the conv weights
 ])
 def test_decode_rejects(K, over, status):
     assert _decode_call(K, **over) == status
@@ -110,6 +114,8 @@ def test_conv_rejects(K):
     assert call(y=BASE + 3 * GAP + 2) == K.KDA_ERR_ALIGNMENT
     assert call(M=0) == K.KDA_ERR_INVALID_ARG
     assert call(cd=0) == K.KDA_ERR_UNSUPPORTED
+    assert call(c=BASE + 16) == K.KDA_ERR_INVALID_ARG          # cache overlaps x
+    assert call(c=BASE + GAP + 16) == K.KDA_ERR_INVALID_ARG    # cache inside the weights
     assert call(y=BASE + 16) == K.KDA_ERR_INVALID_ARG   # y overlaps x
 
 
@@ -179,9 +185,38 @@ def _layer_call(K, **over):
     (dict(x=None), 1), (dict(f=None), 1), (dict(A=None), 1), (dict(T=0), 1), (dict(chunk=32), 2),
     (dict(dk=64), 2), (dict(cd=0), 2), (dict(og=BASE + 9 * GAP), 1),  # out_gate without weight
     (dict(f=BASE + 3 * GAP + 4), 3), (dict(state=BASE + 2 * GAP), 1),  # state aliases the cache
+    (dict(y=BASE + GAP + 16), 1),          # y inside the conv weights
+    (dict(cache=BASE + 4 * GAP), 1),       # cache aliases A_log
+    (dict(state=BASE + 5 * GAP + 16), 1),  # state overlaps dt_bias
 ])
 def test_layer_rejects(K, over, status):
     assert _layer_call(K, **over) == status
+
+
+def _fused_call(K, **over):
+    a = dict(x=BASE, xd=K.KDA_BF16, w=BASE + GAP, cache=BASE + 2 * GAP, cd=K.KDA_BF16,
+             f=BASE + 3 * GAP, A=BASE + 4 * GAP, bias=BASE + 5 * GAP, lb=-5.0,
+             beta=BASE + 6 * GAP, state=BASE + 7 * GAP, sd=K.KDA_F32, scale=1.0,
+             og=BASE + 8 * GAP, nw=BASE + 9 * GAP, neps=1e-5, y=BASE + 10 * GAP,
+             M=4, H=64, dk=128, dv=128)
+    a.update(over)
+    return K.lib().kda_decode_step_fused(a["x"], a["xd"], a["w"], a["cache"], a["cd"], a["f"],
+                                         a["A"], a["bias"], a["lb"], a["beta"], a["state"],
+                                         a["sd"], a["scale"], a["og"], a["nw"], a["neps"],
+                                         a["y"], a["M"], a["H"], a["dk"], a["dv"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(A=None), 1), (dict(bias=None), 1), (dict(nw=None), 1),  # out_gate without weight
+    (dict(og=BASE + 8 * GAP + 4), 3), (dict(dk=64), 2),
+    (dict(y=BASE + 4 * GAP), 1),           # y aliases A_log
+    (dict(cache=BASE + 5 * GAP + 16), 1),  # cache overlaps dt_bias
+    (dict(state=BASE + 9 * GAP), 1),       # state aliases the norm weight
+    (dict(y=BASE + 8 * GAP + 16), 1),      # y overlaps the output gate
+    (dict(y=BASE + 3 * GAP + 16), 1),      # y overlaps the gate input
+])
+def test_fused_rejects(K, over, status):
+    assert _fused_call(K, **over) == status
 
 
 def test_plain_c_caller(K, tmp_path):
