@@ -75,3 +75,49 @@ def test_cuda_error_surfaces_as_status_without_a_gpu():
     assert st == kda.KDA_ERR_CUDA
     assert L.kda_last_cuda_error() != 0
     assert kda.kda_status_string(st) == "KDA_ERR_CUDA"
+
+
+def test_valid_calls_pass_every_host_check_without_a_gpu():
+    """A valid call of every entry point gets past all host-side checks
+    (null pointers, sizes, alignment, overlaps) and only then fails, at the
+    CUDA runtime, with KDA_ERR_CUDA: the checks reject nothing valid. Fake,
+    disjoint, 16-byte aligned addresses are never dereferenced."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful (and only safe: the calls would launch) without a GPU")
+    from linear_attention_decode_step_gb300 import build
+    build.build()
+    from linear_attention_decode_step_gb300 import kda
+    L = kda.lib()
+    A = [(1 << 40) + i * (1 << 34) for i in range(12)]   # disjoint fake buffers
+    BF, F = kda.KDA_BF16, kda.KDA_F32
+    calls = {
+        "kda_conv_step": lambda: L.kda_conv_step(A[0], BF, A[1], A[2], BF, A[3], 2, 512, None),
+        "kda_decode_step": lambda: L.kda_decode_step(A[0], BF, A[1], A[2], BF, A[3], A[4], A[5],
+                                                     BF, 1.0, A[6], 2, 4, 128, 128, None),
+        "kda_decode_step_config": lambda: L.kda_decode_step_config(
+            A[0], F, A[1], A[2], F, A[3], A[4], A[5], F, 1.0, A[6], 2, 4, 128, 128,
+            kda.KDA_DECODE_CLUSTER, 32, 128, None),
+        "kda_decode_step_fused": lambda: L.kda_decode_step_fused(
+            A[0], BF, A[1], A[2], BF, A[3], A[4], A[5], -5.0, A[6], A[7], F, 1.0, A[8], A[9],
+            1e-5, A[10], 2, 4, 128, 128, None),
+        "kda_decode_step_fused (no norm)": lambda: L.kda_decode_step_fused(
+            A[0], BF, A[1], A[2], BF, A[3], A[4], A[5], -5.0, A[6], A[7], F, 1.0, None, None,
+            1e-5, A[10], 2, 4, 128, 128, None),
+        "kda_decode_tokens": lambda: L.kda_decode_tokens(A[0], BF, A[1], A[2], BF, A[3], A[4],
+                                                         A[5], F, 1.0, A[6], 2, 5, 4, 128, 128,
+                                                         None),
+        "kda_chunk_prefill": lambda: L.kda_chunk_prefill(A[0], A[1], A[2], BF, A[3], A[4], A[5],
+                                                         A[6], 1.0, 2, 70, 4, 128, 128, 64, None),
+        "kda_chunk_prefill_config (SIMT)": lambda: L.kda_chunk_prefill_config(
+            A[0], A[1], A[2], F, A[3], A[4], A[5], A[6], 1.0, 2, 70, 4, 128, 128, 64,
+            kda.KDA_PREFILL_SIMT, None),
+        "kda_prefill_layer": lambda: L.kda_prefill_layer(
+            A[0], BF, A[1], A[2], BF, A[3], A[4], A[5], -5.0, A[6], A[7], 1.0, A[8], A[9], 1e-5,
+            A[10], 2, 70, 4, 128, 128, 64, None),
+        "kda_prefill_layer (no norm)": lambda: L.kda_prefill_layer(
+            A[0], F, A[1], A[2], F, A[3], A[4], A[5], -5.0, A[6], A[7], 1.0, None, None, 1e-5,
+            A[10], 2, 70, 4, 128, 128, 64, None),
+    }
+    for name, call in calls.items():
+        assert call() == kda.KDA_ERR_CUDA, name
