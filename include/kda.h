@@ -104,7 +104,8 @@ kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w,
  *                            unrounded updated state; only the store rounds.
  *   scale       multiplies the readout (1.0 reproduces Eq. 1)
  *   o           [M, H, dv]   FP32 output
- *   dk = dv = 128 (other sizes return KDA_ERR_UNSUPPORTED); 1 <= M, H <= 65535.
+ *   dk = dv = 128 (other sizes return KDA_ERR_UNSUPPORTED); 1 <= M, H <= 65535
+ *   and M * H <= 2^30 (KDA_ERR_UNSUPPORTED beyond).
  * The buffers the call writes (o, state, conv_cache) must not overlap each
  * other or any input; an overlap returns KDA_ERR_INVALID_ARG.
  */
@@ -221,7 +222,8 @@ typedef enum {
  *                           and after the last token on return (in place)
  *   o        [M, T, H, dv]  FP32 output, o_t = scale * S_t^T q_t
  *   chunk    tokens per chunk: 64 (other values return KDA_ERR_UNSUPPORTED)
- *   dk = dv = 128; 1 <= M, H <= 65535; T >= 1 (a ragged last chunk is fine).
+ *   dk = dv = 128; 1 <= M, H <= 65535, M * H <= 2^30; T >= 1 (a ragged last
+ *   chunk is fine).
  * Numerical domain: every per-token log(alpha) above about -5.4 (the model's
  * gate keeps it above -5), so that decay factors over a 16-token block stay
  * inside FP32.

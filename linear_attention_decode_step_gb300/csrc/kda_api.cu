@@ -21,6 +21,9 @@ kda_status cuda_status(cudaError_t e) {
     return KDA_ERR_CUDA;
 }
 
+// most (stream, head) units one call may cover (2^30; far beyond any GPU's memory)
+constexpr long long kMaxUnits = 1LL << 30;
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool valid_dtype(int t) { return t == KDA_F32 || t == KDA_BF16; }
@@ -62,7 +65,8 @@ kda_status check_decode(const void *x, int x_dtype, const float *conv_w, void *c
         return KDA_ERR_INVALID_ARG;
     if (dk != kda::kHeadDim || dv != kda::kHeadDim) return KDA_ERR_UNSUPPORTED;
     if (cache_dtype != x_dtype) return KDA_ERR_UNSUPPORTED;
-    if (M > 65535 || H > 65535) return KDA_ERR_UNSUPPORTED;
+    // the kernels count (stream, head) units in 32-bit integers
+    if (M > 65535 || H > 65535 || (long long)M * H > kMaxUnits) return KDA_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_cache) || !aligned16(alpha) ||
         !aligned16(beta) || !aligned16(state) || !aligned16(o))
         return KDA_ERR_ALIGNMENT;
@@ -86,7 +90,8 @@ kda_status check_prefill(const void *q, const void *k, const void *v, int qkv_dt
         return KDA_ERR_INVALID_ARG;
     if (!valid_dtype(qkv_dtype)) return KDA_ERR_INVALID_ARG;
     if (dk != kda::kHeadDim || dv != kda::kHeadDim || chunk != 64) return KDA_ERR_UNSUPPORTED;
-    if (M > 65535 || H > 65535) return KDA_ERR_UNSUPPORTED;
+    // the kernels count (stream, head) units in 32-bit integers
+    if (M > 65535 || H > 65535 || (long long)M * H > kMaxUnits) return KDA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) ||
         !aligned16(beta) || !aligned16(state) || !aligned16(o))
         return KDA_ERR_ALIGNMENT;
@@ -235,7 +240,8 @@ kda_status kda_prefill_layer(const void *x, int x_dtype, const float *conv_w, vo
     if (!valid_dtype(x_dtype) || !valid_dtype(cache_dtype)) return KDA_ERR_INVALID_ARG;
     if (dk != kda::kHeadDim || dv != kda::kHeadDim || chunk != 64) return KDA_ERR_UNSUPPORTED;
     if (cache_dtype != x_dtype) return KDA_ERR_UNSUPPORTED;
-    if (M > 65535 || H > 65535) return KDA_ERR_UNSUPPORTED;
+    // the kernels count (stream, head) units in 32-bit integers
+    if (M > 65535 || H > 65535 || (long long)M * H > kMaxUnits) return KDA_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_cache) || !aligned16(gate_f) ||
         !aligned16(A_log) || !aligned16(dt_bias) || !aligned16(beta) || !aligned16(state) ||
         !aligned16(y) || (out_gate && !aligned16(out_gate)) ||

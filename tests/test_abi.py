@@ -74,7 +74,8 @@ def test_decode_misaligned(K, field):
 @pytest.mark.parametrize("over,status", [
     (dict(M=0), 1), (dict(H=0), 1), (dict(M=-3), 1), (dict(dk=0), 1),
     (dict(dk=64), 2), (dict(dv=64), 2), (dict(dk=256, dv=256), 2),
-    (dict(M=70000), 2), (dict(xd=7), 1), (dict(sd=-1), 1), (dict(cd=5), 1),
+    (dict(M=70000), 2), (dict(M=65535, H=65535), 2),  # M * H beyond 2^30
+    (dict(xd=7), 1), (dict(sd=-1), 1), (dict(cd=5), 1),
     (dict(cd=0), 2),                       # cache dtype must equal x dtype
     (dict(o=BASE + 5 * GAP + 1024), 1),    # o inside the state buffer
     (dict(cache=BASE + 5 * GAP), 1),       # cache aliases the state
@@ -141,6 +142,7 @@ def _prefill_call(K, **over):
     (dict(q=None), 1), (dict(o=None), 1), (dict(state=None), 1), (dict(T=0), 1),
     (dict(M=0), 1), (dict(chunk=0), 1), (dict(qd=3), 1),
     (dict(chunk=32), 2), (dict(dk=64), 2), (dict(dv=256), 2), (dict(H=70000), 2),
+    (dict(M=40000, H=40000), 2),           # M * H beyond 2^30
     (dict(alpha=BASE + 3 * GAP + 8), 3), (dict(o=BASE + 6 * GAP + 4), 3),
     (dict(o=BASE + 16), 1),                 # o overlaps q
     (dict(state=BASE + 3 * GAP + 64), 1),   # state inside alpha
