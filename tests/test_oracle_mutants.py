@@ -133,3 +133,39 @@ def test_tokens_mutant_is_caught(kind, monkeypatch):
     monkeypatch.setattr(oracle, "decode_tokens", _tokens_variant(kind))
     with pytest.raises(AssertionError):
         tp.test_tokens_equal_convolution_then_chunked_form(5)
+
+
+# Planted mistakes in the chunked WY / UT form ("GLM-5.3 deep dive" 8.2.5,
+# Eq. 6-9): each one replaces one line of a copy of oracle.chunk_prefill's
+# source, and the pin that the chunked form reproduces the sequential
+# recurrence must fail. (Keeping the diagonal in A is not among them: the
+# forward substitution reads only A's strictly lower part, so that change
+# computes the same thing.)
+CHUNK_MUTANTS = {
+    "exclusive_cumsum": ("G = np.cumsum(np.log(alpha[m, c0:c1, h]), axis=0)",
+                         "G = np.cumsum(np.log(alpha[m, c0:c1, h]), axis=0)"
+                         " - np.log(alpha[m, c0:c1, h])"),
+    "Ki_grown_not_divided": ("Ki = K * np.exp(-G)", "Ki = K * np.exp(G)"),
+    "A_without_beta": ("A = np.tril(b[:, None] * (Kd @ Ki.T), -1)",
+                       "A = np.tril(Kd @ Ki.T, -1)"),
+    "O_strictly_lower": ("np.tril(Qd @ Ki.T) @ Delta", "np.tril(Qd @ Ki.T, -1) @ Delta"),
+    "beta_left_of_inverse": ("Mx = _unit_lower_solve(A, np.diag(b))",
+                             "Mx = np.diag(b) @ _unit_lower_solve(A, np.eye(len(b)))"),
+    "W_undecayed": ("W, U = Mx @ Kd, Mx @ V", "W, U = Mx @ K, Mx @ V"),
+    "no_state_decay": ("Sh = np.exp(G[-1])[:, None] * Sh +", "Sh = Sh +"),
+    "Kdec_from_chunk_start": ("(np.exp(G[-1] - G) * K).T", "(np.exp(-G) * K).T"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHUNK_MUTANTS))
+def test_chunked_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+    old, new = CHUNK_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(oracle.chunk_prefill))
+    assert src.count(old) == 1, "mutation site not found: " + name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "chunk_prefill_mutant", "exec"), ns)
+    monkeypatch.setattr(oracle, "chunk_prefill", ns["chunk_prefill"])
+    with pytest.raises(AssertionError):
+        pins.test_chunked_equals_sequential(65, 16)
