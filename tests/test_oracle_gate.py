@@ -115,6 +115,22 @@ def test_norm_gate_zero_halves_and_heads_independent():
     np.testing.assert_array_equal(y2[0, 0], y_half[0, 0])
 
 
+def test_norm_eps_inside_root():
+    """The eps of the gated RMSNorm sits inside the root (FusedRMSNormGated,
+    eps 1e-5, "GLM-5.3 deep dive" 8.2.4 notes). A constant vector o = c has
+    mean(o^2) = c^2, so it normalises to c / sqrt(c^2 + eps): with c^2 = eps
+    that is 1/sqrt(2), with c^2 = 3 eps it is sqrt(3)/2. The output gate at
+    0 gives sigmoid(0) = 1/2 exactly and w = 1. With eps outside the root,
+    c / (|c| + eps), both would be within 0.4 % of 1/2 instead: 41 % off the
+    first value and 15 % off the second."""
+    eps = oracle.NORM_EPS
+    for c2, want in ((eps, 0.5 / math.sqrt(2.0)), (3.0 * eps, 0.25 * math.sqrt(3.0))):
+        for sign in (1.0, -1.0):
+            o = np.full((1, 1, 128), sign * math.sqrt(c2))
+            y = oracle.gated_rmsnorm(o, np.zeros(o.shape), np.ones(128), eps=eps)
+            np.testing.assert_allclose(y, sign * want, rtol=1e-12)
+
+
 def test_norm_eps_keeps_zero_finite():
     y = oracle.gated_rmsnorm(np.zeros((1, 1, 8)), np.zeros((1, 1, 8)), np.ones(8))
     assert np.all(y == 0.0)

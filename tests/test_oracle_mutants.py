@@ -38,6 +38,7 @@ GATE_MUTANTS = {
     "gate_sign": ("double g = lb / (1.0 + exp(-z));", "double g = lb / (1.0 + exp(z));"),
     "gate_log_space": ("alpha[i] = exp(g);", "alpha[i] = g;"),
     "norm_sum_not_mean": ("sqrt(ss / dv + eps)", "sqrt(ss + eps)"),
+    "norm_eps_outside_root": ("sqrt(ss / dv + eps)", "(sqrt(ss / dv) + eps)"),
     "norm_weight_dropped": ("oh[j] * r * w[j] /", "oh[j] * r /"),
     "norm_gate_not_sigmoid": ("/ (1.0 + exp(-gh[j]))", "* gh[j]"),
 }
@@ -79,7 +80,7 @@ def test_gate_mutant_is_caught(name, tmp_path, monkeypatch):
                 gp.test_gate_exp_A_scales_the_preactivation, gp.test_gate_bias_per_head_and_channel,
                 gp.test_gate_range, gp.test_norm_constant_vector_and_open_gate,
                 gp.test_norm_scale_invariance_and_unit_rms,
-                gp.test_norm_gate_zero_halves_and_heads_independent):
+                gp.test_norm_gate_zero_halves_and_heads_independent, gp.test_norm_eps_inside_root):
         try:
             pin()
         except Exception:  # an assertion, or e.g. log of a negative "decay"
