@@ -23,7 +23,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -46,7 +45,9 @@ CSRC = os.path.join(ROOT, "linear_attention_decode_step_gb300", "csrc")
 # the kernel kda_decode_step runs for this workload (M*H >= 512 heads) and its source
 DECODE_KERNEL = "kda_decode_stream_kernel"
 DECODE_SRC = os.path.join(CSRC, "kda_decode_stream.cu")
-TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "kda_decode_M32_f32.md")
+# measured DRAM traffic per launch of the decode kernel (ncu, several consecutive
+# launches of a small stack), keyed by the SHA-256 of the kernel's source
+TRAFFIC_DATA = os.path.join(ROOT, "profiles", "kda_decode_traffic.json")
 
 
 # --------------------------------------------------------------------------- sizes
@@ -80,19 +81,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic_per_launch():
-    """dram__bytes_read.sum + dram__bytes_write.sum per launch from the
-    committed ncu summary, if it was taken on the current decode kernel."""
+def ncu_traffic_per_launch(M: int, state_dtype: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch of the decode
+    kernel at this M and state dtype, from the committed measurement, if it
+    was taken on the current kernel source (else None)."""
     try:
-        text = open(TRAFFIC_NOTE).read()
-    except OSError:
+        with open(TRAFFIC_DATA) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
         return None
     src = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
-    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != src:
+    if data.get("kernel_source_sha256") != src:
         return None
-    return float(m_tr.group(1))
+    for row in data.get("per_launch", []):
+        if row.get("M") == M and row.get("state_dtype") == state_dtype:
+            return float(row["dram_bytes"])
+    return None
 
 
 # --------------------------------------------------------------------------- clocks
@@ -368,6 +372,44 @@ def sweep(args):
             torch.cuda.empty_cache()
 
 
+SWEEP_M = (1, 8, 16, 32, 64)
+SWEEP_DTYPES = ("f32", "bf16")
+
+
+def sweep_object(torch, kda, inputs, dev, layers, x_dtype, peak, peak_kind, gpu_id):
+    """The 34-layer stack at every M of SWEEP_M with FP32 and BF16 state (one
+    CUDA graph of the stack's launches per step, a bounded number of steps per
+    point, SM clocks sampled across the sweep). Returns the `sweep` object of
+    the bench line."""
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    points = []
+    for sd in SWEEP_DTYPES:
+        for M in SWEEP_M:
+            stack = DecodeStack(torch, kda, inputs, M, layers, sd, x_dtype, dev, replicate=True)
+            K = max(20, min(300, 3000 // M))
+            ms = time_graph(stack, K, 3)
+            us = ms / K / layers * 1e3
+            gbs = state_bytes_per_launch(M, sd) / (us * 1e-6) / 1e9
+            ab = algorithmic_bytes_per_launch(M, sd, x_dtype)
+            points.append({"M": M, "state_dtype": sd, "steps": K,
+                           "ms_per_stack": ms / K, "us_per_layer": us, "state_gbs": gbs,
+                           "state_frac_of_%s_hbm" % peak_kind: gbs / peak,
+                           "algorithmic_gbs": ab / (us * 1e-6) / 1e9,
+                           "roofline_frac": ab / (us * 1e-6) / 1e9 / peak})
+            del stack
+            torch.cuda.empty_cache()
+    return {"workload": "%d-layer KDA decode stack (one token per step, every layer its own "
+                        "state and conv cache, %s q/k/v), M x 64 heads x 128x128 state, for "
+                        "M in %s and FP32 / BF16 state storage" % (layers, x_dtype.upper(),
+                                                                    list(SWEEP_M)),
+            "kernel": DECODE_KERNEL, "launch": "one CUDA graph of %d kda_decode_step launches "
+                                                "per step; CUDA events around the replays" % layers,
+            "l2": "inputs larger than L2 from M = 8 on (M = 1: 8.4 MB of state per layer, "
+                  "285 MB per step for FP32)",
+            "points": points, "clocks": clocks.stop()}
+
+
 def time_e2e(stack: DecodeStack, K: int, W: int, barrier):
     """K steps through the public API with host buffers: every step copies its
     inputs (x, alpha, beta of all layers) in from pinned host memory, runs the
@@ -511,7 +553,7 @@ def prefill_layer_bytes(M, T, H, x_bytes=2, norm=True):
 def prefill_summary(ms, M, T, peak_hbm, peak_bf16, kernel_name):
     gb = prefill_bytes(M, T, H) / 1e9
     tflop = prefill_flops(M, T, H) / 1e12
-    tf32_peak = peak_bf16 / 2   # TF32 dense rate is half the BF16 rate (1.1 vs 2.25 PF nominal)
+    tf32_peak = peak_bf16 * 1.1 / 2.25   # measured BF16 x the nominal TF32 / BF16 ratio
     return {
         "workload": "chunked prefill, M=%d streams x T=%d tokens x %d heads, 128x128 FP32 state, "
                     "BF16 q/k/v, chunk 64" % (M, T, H),
@@ -760,7 +802,7 @@ def own_arm(args, rank: int, world: int, local_rank: int):
     mean_launch_ms = total_ms / (K * args.layers)   # launch-to-launch, gaps included
     peak, peak_kind = measured_peak()
     achieved = ab / (mean_launch_ms * 1e-3) / 1e9
-    traffic = ncu_traffic_per_launch() if (args.M == 32 and args.state_dtype == "f32") else None
+    traffic = ncu_traffic_per_launch(args.M, args.state_dtype)
 
     if rank != 0:
         return
@@ -827,6 +869,9 @@ def own_arm(args, rank: int, world: int, local_rank: int):
             "fp32_peak_kind": "152 SMs x 128 FP32 lanes x 2 x SM clock (%s MHz)"
                               % ("sampled %.0f" % mhz if mhz else "max 2070"),
             "per_T": rows}
+    if not args.no_sweep:
+        line["sweep"] = sweep_object(torch, kda, inputs, dev, args.layers, args.x_dtype, peak,
+                                     peak_kind, gpu_uuid(torch, dev))
     if world == 1 and not args.no_cpu_baseline:
         gbs1, n1, el1 = oracle_decode_sample(stack.host0, args.cpu_seconds / 3)
         gbs, n, el, cores = oracle_all_cores_sample(2 * args.cpu_seconds / 3)
@@ -878,6 +923,8 @@ def main():
     ap.add_argument("--sweep-m", default="1,8,16,32,64")
     ap.add_argument("--sweep-dtypes", default="f32,bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sweep object (the stack at M = 1..64, FP32 and BF16 state)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -285,13 +285,17 @@ kda_status kda_chunk_prefill_config(const void *q, const void *k, const void *v,
 
 /*
  * kda_device_error — waits for `stream` (cudaStream_t as void*, NULL = legacy
- * default stream), then reads and clears the library's device error word.
- * Returns KDA_ERR_TIMEOUT if a kernel gave up a bounded device-side wait since
- * the last call (its outputs are then incomplete), KDA_ERR_ALIGNMENT if the
- * tensor-core prefill found its dynamic shared memory not 1024-byte aligned
- * (it then returns without computing; the swizzled tensor copies need that
- * alignment), KDA_ERR_CUDA if the wait or the read failed, KDA_OK otherwise.
- * The error word is shared by all streams of the device.
+ * default stream), then reads the library's device error words (one per
+ * kernel family) and clears those that were set. Returns, in this order of
+ * precedence: KDA_ERR_CUDA if the wait, a read or a clear failed (a failed
+ * read clears nothing); KDA_ERR_TIMEOUT if a kernel gave up a bounded
+ * device-side wait since the words were last cleared (its outputs are then
+ * incomplete); KDA_ERR_ALIGNMENT if the tensor-core prefill found its dynamic
+ * shared memory not 1024-byte aligned (it then returns without computing; the
+ * swizzled tensor copies need that alignment); KDA_OK otherwise.
+ * The words are per device, shared by every stream and every caller of the
+ * library in the process: callers that share a device and want their own
+ * errors must serialise their calls of kda_device_error with their launches.
  */
 kda_status kda_device_error(void *stream);
 

@@ -78,6 +78,43 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     return LIB
 
 
+def build_variant(tag: str, defines: list[str], only: list[str]) -> str:
+    """A second build of the library for tests: the sources named in `only`
+    (file names under csrc/) compiled with extra preprocessor definitions
+    (`defines`, e.g. ["KDA_WAIT_BUDGET=0"]), linked with the regular objects
+    of the other sources into libkda_gb300_<tag>.so next to the regular
+    library. Returns its path. The regular library is built first."""
+    build()
+    cc = nvcc()
+    obj_dir = os.path.join(PKG, "_build_" + tag)
+    os.makedirs(obj_dir, exist_ok=True)
+    flags = NVCC_FLAGS + ["-D" + d for d in defines]
+    lib = os.path.join(PKG, "libkda_gb300_%s.so" % tag)
+
+    def obj_for(src: str) -> str:
+        name = os.path.basename(src)
+        if name in only:
+            obj = os.path.join(obj_dir, name[:-3] + ".o")
+            res = subprocess.run([cc] + flags + ["-c", src, "-o", obj], capture_output=True, text=True)
+            if res.returncode != 0:
+                raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, res.stdout, res.stderr))
+            return obj
+        return os.path.join(OBJ_DIR, name[:-3] + ".o")
+
+    srcs = sources()
+    missing = [n for n in only if os.path.join(CSRC, n) not in srcs]
+    if missing:
+        raise ValueError("no such source: %s" % ", ".join(missing))
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(obj_for, srcs))
+    tmp = lib + ".tmp%d" % os.getpid()
+    res = subprocess.run([cc] + ARCH + ["-shared", "-o", tmp] + objs, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     v = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas" in sys.argv else None

@@ -351,15 +351,21 @@ kda_status kda_decode_tokens(const void *x, int x_dtype, const float *conv_w, vo
 kda_status kda_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_status(e);
-    unsigned int code = 0, code2 = 0, code3 = 0;
-    e = kda::take_stream_error(&code);
+    // all three words are read before any is cleared, so a failed read loses
+    // nothing; then the words that were set are cleared
+    unsigned int ws = 0, wp = 0, wt = 0;
+    e = kda::read_stream_error(&ws);
+    if (e == cudaSuccess) e = kda::read_prefill_error(&wp);
+    if (e == cudaSuccess) e = kda::read_tokens_error(&wt);
     if (e != cudaSuccess) return cuda_status(e);
-    e = kda::take_prefill_error(&code2);
+    if (ws) e = kda::clear_stream_error();
+    if (e == cudaSuccess && wp) e = kda::clear_prefill_error();
+    if (e == cudaSuccess && wt) e = kda::clear_tokens_error();
     if (e != cudaSuccess) return cuda_status(e);
-    e = kda::take_tokens_error(&code3);
-    if (e != cudaSuccess) return cuda_status(e);
-    if (code2 & kda::kPrefillErrMisaligned) return KDA_ERR_ALIGNMENT;
-    return (code | code2 | code3) ? KDA_ERR_TIMEOUT : KDA_OK;
+    // a wait that gave up takes precedence over the prefill's alignment report
+    if (ws || wt || (wp & ~kda::kPrefillErrMisaligned)) return KDA_ERR_TIMEOUT;
+    if (wp & kda::kPrefillErrMisaligned) return KDA_ERR_ALIGNMENT;
+    return KDA_OK;
 }
 
 }  // extern "C"

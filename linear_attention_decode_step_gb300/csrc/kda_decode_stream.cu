@@ -54,10 +54,13 @@
 // Each conv-cache channel belongs to exactly one head, so the cache is read
 // (by the bulk copy) and rewritten (by the consumer) by one CTA only.
 //
-// Every mbarrier wait is bounded (about two seconds of clock cycles); on
-// timeout the thread sets the device error word, waits once more (bounded)
-// for the copy it was waiting on, and returns. kda_device_error() reports it
-// on the host.
+// Every mbarrier wait is bounded (about two seconds of clock cycles). A
+// thread whose wait gives up sets the device error word and skips its writes
+// to global memory; the group's next barrier ANDs every thread's outcome, so
+// the whole group leaves the loop together. At exit the CTA meets once more
+// and one thread waits (bounded) for the latest bulk copy into every stage,
+// so nothing lands in shared memory after the CTA is gone.
+// kda_device_error() reports the error word on the host.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -76,7 +79,6 @@ namespace {
 
 constexpr int DK = kHeadDim;
 constexpr float kL2Eps = 1e-6f;
-constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s at 2 GHz)
 constexpr int kSmemLimit = 232448;               // 227 KiB opt-in per CTA
 constexpr int kWarps = 16;
 
@@ -107,7 +109,7 @@ struct Cfg {
     static constexpr int NRM_F = AB_F + 2 * DK;  // [4] norm partials | q.q | q.k | pad
     static constexpr int WORK_F = NRM_F + 8;
     static constexpr int WORK_BYTES = WORK_F * 4;
-    static constexpr int BAR_BYTES = 2 * 8 * 8;        // full[8], issued[8]
+    static constexpr int BAR_BYTES = 2 * 8 * 8 + 8 * 4;  // full[8], issued[8], fills[8]
     static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
     static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
     static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
@@ -203,6 +205,9 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
     uint64_t *issued = full + 8;
+    // bulk copies issued into each stage so far (written by the issuing
+    // thread before it arrives on `issued`; read after the exit barrier)
+    volatile uint32_t *fills = reinterpret_cast<volatile uint32_t *>(issued + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
@@ -215,6 +220,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         for (int s = 0; s < C::NST; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&issued[s], 1);
+            fills[s] = blockIdx.x + s * gridDim.x < n_units ? 1u : 0u;  // the first fills, below
         }
         ptx::fence_mbar_init();
     }
@@ -304,12 +310,12 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         const int un = u + G * gridDim.x;
         if (un < n_units) prefetch(un);
 
-        if ((n > 0 && !ptx::mbar_wait(&issued[s], (n - 1) & 1, kWaitBudget)) ||
-            !ptx::mbar_wait(&full[s], n & 1, kWaitBudget)) {
-            raise_error(4u);
-            ptx::mbar_wait(&full[s], n & 1, kWaitBudget);
-            return;
-        }
+        // the stage's refill was issued, then its bytes landed; a thread whose
+        // wait gives up reads no further data of this head and writes nothing
+        // (the group leaves together at barrier 1)
+        const bool landed = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                            ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+        if (!landed) raise_error(4u);
         const unsigned char *st = smem + s * C::STAGE;
         const TS *Ss = reinterpret_cast<const TS *>(st);
         const float *al = reinterpret_cast<const float *>(st + C::A_OFF);
@@ -335,23 +341,25 @@ kda_decode_stream_kernel(const DecodeArgs a) {
 
         // (b) conv + SiLU of the head's 384 channels (q, k, v)
         const size_t cbase = (size_t)m * 9 * D + (size_t)h * DK;
-        if (c0 < 3 * DK) {
+        if (landed && c0 < 3 * DK) {
             const int X = c0 / DK, ch = c0 % DK;
             const float y = conv_stage(w0, cs, xs, X, ch, cache + cbase + 3 * X * D + ch, D);
             if (X < 2) qkb[X * DK + ch] = y;
             else vb[ch] = y;
         }
-        if (c1 < 3 * DK) {
+        if (landed && c1 < 3 * DK) {
             const int X = c1 / DK, ch = c1 % DK;
             const float y = conv_stage(w1, cs, xs, X, ch, cache + cbase + 3 * X * D + ch, D);
             if (X < 2) qkb[X * DK + ch] = y;
             else vb[ch] = y;
         }
-        ptx::named_bar_sync(bar_id, C::GT);  // barrier 1: stage read; q, k, v visible
+        // barrier 1: stage read; q, k, v visible; every thread's wait succeeded
+        if (!ptx::named_bar_and(bar_id, C::GT, landed)) break;
         if (ct == 0) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;  // refill with head i + NST
             if (ur < n_units) {
                 load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                fills[s] = fills[s] + 1u;
                 ptx::mbar_arrive(&issued[s]);
                 const int up = ur + P * gridDim.x;
                 if (P > 0 && up < n_units) prefetch_head<TS>(a, up);
@@ -503,6 +511,19 @@ kda_decode_stream_kernel(const DecodeArgs a) {
             __stcs(reinterpret_cast<uint4 *>(Sg + (size_t)row * DK), Strip<TS>::pack(nv));
         }
     }
+
+    // Exit. After a wait gave up, bulk copies into some stages may still be
+    // in flight; once both groups are here no thread issues another one, so
+    // waiting for the latest fill of every stage covers them all (in a run
+    // without errors each of those has landed and was consumed: the waits
+    // return at once).
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const uint32_t f = fills[s];
+            if (f > 0) ptx::mbar_wait(&full[s], (f - 1) & 1, ptx::kDrainBudget);
+        }
+    }
 }
 
 template <typename TS, typename TX, int G, bool GATE, bool NORM>
@@ -564,12 +585,13 @@ cudaError_t launch_decode_stream_fused(const DecodeArgs &a, int x_dtype, int sta
     return launch_fused<float, float>(a, stream);
 }
 
-cudaError_t take_stream_error(unsigned int *code) {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_stream_error, sizeof(unsigned int));
-    if (e != cudaSuccess) return e;
-    if (*code) e = cudaMemcpyToSymbol(g_stream_error, &zero, sizeof(unsigned int));
-    return e;
+cudaError_t read_stream_error(unsigned int *code) {
+    return cudaMemcpyFromSymbol(code, g_stream_error, sizeof(unsigned int));
+}
+
+cudaError_t clear_stream_error() {
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_stream_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace kda

@@ -4,10 +4,12 @@
 // read order of section 8.2.6, readout o = w + d (k.q)), token after token,
 // as fla's fused-recurrent mode does for short inputs (section 8.2.5).
 //
-// Every mbarrier wait is bounded (about two seconds of clock cycles); on
-// timeout the thread sets this file's device error word, waits once more
-// (bounded) for the copy it was waiting on, and returns. kda_device_error()
-// reports it on the host.
+// Every mbarrier wait is bounded (about two seconds of clock cycles). A
+// thread whose wait gives up sets this file's device error word; the group's
+// next barrier ANDs every thread's outcome, so the whole group leaves the
+// loop together, before anything of that head is written. At exit the CTA
+// meets once more and one thread waits (bounded) for the latest bulk copy
+// into every stage. kda_device_error() reports the error word on the host.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -26,7 +28,6 @@ namespace {
 
 constexpr int DK = kHeadDim;
 constexpr float kL2Eps = 1e-6f;
-constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s at 2 GHz)
 constexpr int kSmemLimit = 232448;               // 227 KiB opt-in per CTA
 constexpr int kWarps = 16;
 
@@ -60,8 +61,9 @@ __device__ __forceinline__ void raise_error(unsigned int code) { atomicOr(&g_tok
 //    ahead of their convolution (one token ahead left the load latency
 //    exposed: about a sixth of the time at T = 8).
 // ---------------------------------------------------------------------------
-template <typename TS, typename TX, int G>
+template <typename TS, typename TX, int G_>
 struct TokCfg {
+    static constexpr int G = G_;
     static constexpr int CWARPS = kWarps / G;          // warps per group (16 columns each)
     static constexpr int GT = CWARPS * 32;
     static constexpr int THREADS = kWarps * 32;
@@ -76,7 +78,7 @@ struct TokCfg {
     static constexpr int W_OFF = 2 * BUF_F * 4;
     static constexpr int WIN_OFF = W_OFF + 3 * DK * 16;
     static constexpr int WORK_BYTES = WIN_OFF + ((9 * DK * (int)sizeof(TX) + 15) / 16) * 16;
-    static constexpr int BAR_BYTES = 2 * 8 * 8;
+    static constexpr int BAR_BYTES = 2 * 8 * 8 + 8 * 4;  // full[8], issued[8], fills[8]
     static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
     static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
     static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
@@ -140,6 +142,19 @@ __device__ __forceinline__ float conv_silu(const float4 w, const TX (&win)[3], T
     return __fdividef(pre, 1.0f + __expf(-pre));
 }
 
+// The exit wait: for the latest bulk copy into every stage to have landed
+// (one thread; in a run without errors they all have, and it returns at
+// once). Kept out of line so the kernel's loop keeps its registers.
+template <typename C>
+__device__ __noinline__ void drain_fills(unsigned char *smem) {
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + C::G * C::WORK_BYTES);
+    const volatile uint32_t *fills = reinterpret_cast<const volatile uint32_t *>(full + 16);
+    for (int s = 0; s < C::NST; ++s) {
+        const uint32_t f = fills[s];
+        if (f > 0) ptx::mbar_wait(&full[s], (f - 1) & 1, ptx::kDrainBudget);
+    }
+}
+
 template <typename TS, typename TX, int G>
 __global__ void __launch_bounds__(TokCfg<TS, TX, G>::THREADS, 1)
 kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
@@ -147,6 +162,9 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
     uint64_t *issued = full + 8;
+    // bulk copies issued into each stage so far (written by the issuing
+    // thread before it arrives on `issued`; read after the exit barrier)
+    volatile uint32_t *fills = reinterpret_cast<volatile uint32_t *>(issued + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
@@ -158,6 +176,7 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         for (int s = 0; s < C::NST; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&issued[s], 1);
+            fills[s] = blockIdx.x + s * gridDim.x < n_units ? 1u : 0u;  // the first fills, below
         }
         ptx::fence_mbar_init();
     }
@@ -237,12 +256,12 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             beta_m = __ldg(bp + 2 * H);
         }
 
-        if ((n > 0 && !ptx::mbar_wait(&issued[s], (n - 1) & 1, kWaitBudget)) ||
-            !ptx::mbar_wait(&full[s], n & 1, kWaitBudget)) {
-            raise_error(8u);
-            ptx::mbar_wait(&full[s], n & 1, kWaitBudget);
-            return;
-        }
+        // the stage's refill was issued, then its bytes landed (a thread whose
+        // wait gives up goes on to the group barrier below, where the group
+        // leaves together; nothing reaches global memory before it)
+        const bool landed = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                            ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+        if (!landed) raise_error(8u);
         const unsigned char *st = smem + s * C::STAGE;
         const TS *Ss = reinterpret_cast<const TS *>(st);
         const TX *cs = reinterpret_cast<const TX *>(st + C::C_OFF);
@@ -286,11 +305,17 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             if (ct < DK) b[2 * DK + perm_row(ct)] = al;
         };
         convolve(buf, a0, x00, x10);
-        ptx::named_bar_sync(bar_id, C::GT);  // stage read; token 0 in buffer 0
-        if (ct == 0) {
+        // stage read; token 0 in buffer 0; every thread's wait succeeded
+        // (after a wait gave up anywhere in the group: the group finishes this
+        // head without writing anything and without a refill, and the loop's
+        // condition then ends it)
+        const bool go = ptx::named_bar_and(bar_id, C::GT, landed);
+        if (!go) u = n_units;
+        if (ct == 0 && go) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
             if (ur < n_units) {
                 load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                fills[s] = fills[s] + 1u;
                 ptx::mbar_arrive(&issued[s]);
             }
         }
@@ -377,7 +402,7 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             float d = 0.f;
             if (!b2) d = beta * (bc[3 * DK + ocol] - rk * z);
             const float d_o = __shfl_xor_sync(0xffffffffu, d, 16);
-            if (b2) op[(size_t)t * as] = a.scale * (rq * z + d_o * (sqk * rq * rk));
+            if (b2 && go) op[(size_t)t * as] = a.scale * (rq * z + d_o * (sqk * rq * rk));
             // S' = s + k_hat d: k_hat = rk k, so scale d by rk once
             const float dk = d * rk;
             float dd[4];
@@ -399,6 +424,7 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         }
 
         // state out (rounded once, here, for BF16 storage) and the final conv windows
+        if (!go) continue;
         TS *Sg = static_cast<TS *>(a.state) + (size_t)u * DK * DK + col0;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -412,6 +438,12 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
             if (has1) cache[cbase + (size_t)(3 * X1 + j) * D + ch1] = win[j * 3 * DK + c1];
         }
     }
+
+    // Exit: once both groups are here no thread issues another bulk copy, so
+    // waiting for the latest fill of every stage covers any still in flight
+    // after a wait gave up (without errors they have all landed already).
+    __syncthreads();
+    if (threadIdx.x == 0) drain_fills<C>(smem);
 }
 
 template <typename TS, typename TX>
@@ -452,12 +484,13 @@ cudaError_t launch_decode_tokens(const DecodeArgs &a, int T, int x_dtype, int st
     return launch_tokens_typed<float, float>(a, T, stream);
 }
 
-cudaError_t take_tokens_error(unsigned int *code) {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_tokens_error, sizeof(unsigned int));
-    if (e != cudaSuccess) return e;
-    if (*code) e = cudaMemcpyToSymbol(g_tokens_error, &zero, sizeof(unsigned int));
-    return e;
+cudaError_t read_tokens_error(unsigned int *code) {
+    return cudaMemcpyFromSymbol(code, g_tokens_error, sizeof(unsigned int));
+}
+
+cudaError_t clear_tokens_error() {
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_tokens_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace kda

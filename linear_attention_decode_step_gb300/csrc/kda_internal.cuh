@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace kda {
@@ -54,6 +55,16 @@ struct PrefillArgs {
     float norm_eps;
 };
 
+// Encodes a tiled tensor map over a dense row-major tensor whose dims are
+// listed innermost first (dims[0] contiguous; strides follow from the dims),
+// with the given box, zero fill outside the tensor, optionally the 128-byte
+// swizzle, and L2 promotion of the requests to 0: none, 1: 128 bytes,
+// 2: 256 bytes. cudaErrorNotSupported if the driver lacks the encoder,
+// cudaErrorInvalidValue if it rejects the map.
+cudaError_t make_tensor_map(CUtensorMap *map, const void *base, bool bf16, int rank,
+                            const uint64_t *dims, const uint32_t *box, bool swizzle128,
+                            int l2_promotion = 2);
+
 // Chunked prefill on CUDA cores (64-token chunks, 16-token blocks).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, int qkv_dtype, cudaStream_t stream);
 
@@ -66,8 +77,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, int qkv_dtype, cudaStream_t 
 // the gated RMSNorm on every output.
 cudaError_t launch_prefill_layer(const PrefillArgs &a, int x_dtype, cudaStream_t stream);
 
-// Reads and clears the tensor-core prefill's device error word.
-cudaError_t take_prefill_error(unsigned int *code);
+// Reads / clears the tensor-core prefill's device error word.
+cudaError_t read_prefill_error(unsigned int *code);
+cudaError_t clear_prefill_error();
 // Bit of the prefill's error word set when its dynamic shared memory is not
 // 1024-byte aligned (every other bit marks a bounded wait that gave up).
 constexpr unsigned int kPrefillErrMisaligned = 64u;
@@ -99,11 +111,13 @@ cudaError_t launch_decode_tokens(const DecodeArgs &a, int T, int x_dtype, int st
 void default_decode_config(int M, int H, int state_dtype, int *kernel, int *columns,
                            int *threads);
 
-// Reads and clears the streaming kernel's device error word.
-cudaError_t take_stream_error(unsigned int *code);
+// Reads / clears the streaming kernel's device error word.
+cudaError_t read_stream_error(unsigned int *code);
+cudaError_t clear_stream_error();
 
-// Reads and clears the multi-token decode kernel's device error word.
-cudaError_t take_tokens_error(unsigned int *code);
+// Reads / clears the multi-token decode kernel's device error word.
+cudaError_t read_tokens_error(unsigned int *code);
+cudaError_t clear_tokens_error();
 
 // Standalone short conv + SiLU for one token.
 cudaError_t launch_conv(const void *x, int x_dtype, const float *conv_w, void *cache,

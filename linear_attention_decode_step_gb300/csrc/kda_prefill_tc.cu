@@ -55,8 +55,12 @@
 // the [Kd; Qd] region once MMA3 has read it (FP32 q, k are loaded into
 // registers a chunk ahead instead); v of the next chunk arrives in one tensor
 // copy; O leaves through shared memory in one tensor store. Every mbarrier
-// wait is bounded; on timeout the kernel sets the device error word
-// (kda_device_error) and stops.
+// wait is bounded. A thread whose wait gives up sets the device error word
+// (kda_device_error) and carries on to the next CTA-wide barrier, which ANDs
+// every thread's outcome (__syncthreads_and), so the CTA leaves the chunk
+// loop together; on the way out the thread that issued the tensor-core
+// products and the thread that issued the tensor copies wait (bounded) for
+// their last ones, and only then is the tensor memory freed.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -80,7 +84,6 @@ constexpr int DK = kHeadDim;
 constexpr int C = 64;
 constexpr int NT = 512;
 constexpr float kL2Eps = 1e-6f;
-constexpr long long kWaitBudget = 4000000000LL;
 
 // operand tiles (bytes), K-major core-matrix layout
 constexpr uint32_t KB128 = DK * 4;  // one row of a K = 128 tile
@@ -426,22 +429,24 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
     const uint32_t id96 = umma::instr_desc(128, 96, umma::kFmtTF32);
     const uint32_t id64 = umma::instr_desc(128, 64, umma::kFmtTF32);
+    // false once a wait of this thread gave up; folded into the next
+    // CTA-wide barrier, where the whole CTA leaves the loop together
     bool ok = true;
-    int v_pending = 1;  // a tensor copy of v is in flight (completion parity: v_parity)
-    int v_parity = 0;
-    int qka_pending = kTma;  // the same for the staged q, k, alpha
-    int qka_parity = 0;
+    // the loader's tensor copies issued so far (bar[4]: v, bar[5]: q, k,
+    // alpha) and the issuer's last commit (bar index, phase parity), for the
+    // exit path
+    int v_issued = tid == kLoader ? 1 : 0;
+    int qka_issued = tid == kLoader && kTma ? 1 : 0;
+    int last_bar = -1, last_par = 0;
     int phase = 0;
 
-    for (int c0 = 0; c0 < T && ok; c0 += C, phase ^= 1) {
+    for (int c0 = 0; c0 < T; c0 += C, phase ^= 1) {
         // ---------------------------------------------------------- 1. decay, norms
         if constexpr (kTma) {
-            if (!ptx::mbar_wait(&bar[5], phase, kWaitBudget)) {
+            if (!ptx::mbar_wait(&bar[5], phase, ptx::kWaitBudget)) {
                 raise_error(32u);
                 ok = false;
-                break;
             }
-            qka_pending = 0;
             fetch_qka(R, sm, r0, c4);
         }
         // cumulative log2-decay over the half's 32 tokens (lanes rr, then g)
@@ -608,7 +613,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
         }
         if (tid < C) sBeta[tid] = beta_n;
-        __syncthreads();
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
         float rq[4], rk[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -690,6 +698,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                              umma::smem_desc(sbase + T_RB + ks * 256, 128, 8 * KB128), id96, ks > 0,
                              1);
             umma::commit(&bar[0]);
+            last_bar = 0;
+            last_par = phase;
         }
         // under MMA1: Kdec = K e^{G63 - G} = R ed, as the Kdec^T tile
 #pragma unroll
@@ -710,10 +720,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             const float ko[4] = {b0 ? x0 : v4[0], b0 ? v4[1] : x0, b0 ? x1 : v4[2], b0 ? v4[3] : x1};
             st_tile4(sm + T_KDEC, 4 * c4 + ce, 8 * rh + 2 * g + hh, KB64, ko[0], ko[1], ko[2], ko[3]);
         }
-        if (!ptx::mbar_wait(&bar[0], phase, kWaitBudget)) {
+        if (!ptx::mbar_wait(&bar[0], phase, ptx::kWaitBudget)) {
             raise_error(1u);
             ok = false;
-            break;
         }
         umma::fence_after_sync();
 
@@ -757,7 +766,11 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
         }
         umma::fence_before_sync();
-        __syncthreads();  // A, P visible; MMA1 operands may now be overwritten
+        // A, P visible; MMA1 operands may now be overwritten
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
 
         // ---------------------------------------------------------- 4. state-pass operands
         //   Kd = K e^G = L em,   Qd = Lq em   (Kdec^T was written under MMA1)
@@ -780,6 +793,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 umma::mma_ts(tb + TM_D3, tb + TM_S + ks * 8,
                              umma::smem_desc(sbase + T_KQ + ks * 256, 128, 8 * KB128), id128, ks > 0);
             umma::commit(&bar[1]);
+            last_bar = 1;
+            last_par = phase;
         }
         // the next chunk's q, k, alpha (the registers of this one are consumed);
         // issued after the proxy fence above, which would otherwise wait for them
@@ -941,18 +956,19 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             // ------------------------------------------------------ 6. Z = V - Y, decay S
             // (warps 8-15, while warps 0-7 invert): warp w does the units hq6 =
             // 2 ((w - 8) / 4) and + 1 of its lane quarter
-            if (!ptx::mbar_wait(&bar[1], phase, kWaitBudget)) {
+            if (!ptx::mbar_wait(&bar[1], phase, ptx::kWaitBudget)) {
                 raise_error(2u);
                 ok = false;
-                break;
             }
             umma::fence_after_sync();
             // MMA3 has read [Kd; Qd]: the region takes the next chunk's q, k, alpha
-            if (kTma && tid == kLoader && c0 + C < T) issue_qka(c0 + C);
-            if (!ptx::mbar_wait(&bar[4], phase, kWaitBudget)) {
+            if (kTma && tid == kLoader && c0 + C < T && ok) {
+                issue_qka(c0 + C);
+                ++qka_issued;
+            }
+            if (!ptx::mbar_wait(&bar[4], phase, ptx::kWaitBudget)) {
                 raise_error(16u);
                 ok = false;
-                break;
             }
 #pragma unroll 1
             for (int u6 = 0; u6 < 2; ++u6) {
@@ -1014,11 +1030,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
             umma::wait_st();
         }
-        if (kTma && c0 + C < T) {
-            qka_pending = 1;
-            qka_parity = phase ^ 1;
-        }
-        v_pending = 0;
         // the layer form: raw q, k of tokens 29-31 of the next chunk (loaded in phase 4)
         if (!kTma && LAYER && rh == 0 && rr >= 5 && c0 + C < T) {
             float xq[4], xk[4];
@@ -1029,12 +1040,14 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
 
         umma::fence_before_sync();
-        __syncthreads();
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
         umma::fence_after_sync();
-        if (tid == kLoader && c0 + C < T) issue_v(c0 + C);
-        if (c0 + C < T) {
-            v_pending = 1;
-            v_parity = phase ^ 1;
+        if (tid == kLoader && c0 + C < T) {
+            issue_v(c0 + C);
+            ++v_issued;
         }
         if (tid == kIssuer) {
 #pragma unroll 1
@@ -1042,8 +1055,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 umma::mma_ts(tb + TM_D4, tb + TM_Z + ks * 8,
                              umma::smem_desc(sbase + T_M + ks * 256, 128, 8 * KB64), id64, ks > 0);
             umma::commit(&bar[2]);
-            if (!ptx::mbar_wait(&bar[2], phase, kWaitBudget)) {
+            if (!ptx::mbar_wait(&bar[2], phase, ptx::kWaitBudget)) {
                 raise_error(4u);
+                ok = false;
             } else {
                 umma::fence_after_sync();
 #pragma unroll 1
@@ -1055,6 +1069,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                 }
             }
             umma::commit(&bar[3]);
+            last_bar = 3;
+            last_par = phase;
         }
         // the norm's output gate rows of this warp (4 w .. 4 w + 3) and weights, loaded
         // under the state-pass products
@@ -1068,10 +1084,9 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        if (!ptx::mbar_wait(&bar[3], phase, kWaitBudget)) {
+        if (!ptx::mbar_wait(&bar[3], phase, ptx::kWaitBudget)) {
             raise_error(8u);
             ok = false;
-            break;
         }
         umma::fence_after_sync();
 
@@ -1085,7 +1100,10 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             for (int e = 0; e < 16; ++e) sO[(16 * hq + e) * DK + j] = a.scale * o16[e];
         }
         if (NORM) {  // y = o / sqrt(mean o^2 + eps) * w * sigmoid(gate), warp w: rows 4 w .. 4 w + 3
-            __syncthreads();
+            if (!__syncthreads_and(ok)) {
+                ok = false;
+                break;
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t = 4 * warp + i;
@@ -1113,13 +1131,21 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
     }
 
-    // after a timeout, let a tensor copy still in flight land before the CTA's
-    // shared memory goes (bounded as well)
-    if (!ok && v_pending) ptx::mbar_wait(&bar[4], v_parity, kWaitBudget);
-    if (!ok && qka_pending) ptx::mbar_wait(&bar[5], qka_parity, kWaitBudget);
+    // Every thread arrives here (the loop ends, or breaks, for the whole CTA
+    // at once); a wait that gave up after the last CTA-wide barrier of the
+    // loop counts as well.
+    const bool all_ok = __syncthreads_and(ok);
+    // Before the shared and tensor memory go: the last tensor copies into
+    // shared memory and the last tensor-core products have landed (at once
+    // in a run without errors, where each was waited for already).
+    if (tid == kLoader) {
+        if (v_issued > 0) ptx::mbar_wait(&bar[4], (v_issued - 1) & 1, ptx::kDrainBudget);
+        if (qka_issued > 0) ptx::mbar_wait(&bar[5], (qka_issued - 1) & 1, ptx::kDrainBudget);
+    }
+    if (tid == kIssuer && last_bar >= 0) ptx::mbar_wait(&bar[last_bar], last_par, ptx::kDrainBudget);
 
     // state out
-    if (ok) {
+    if (all_ok) {
         for (int c = 32 * hq; c < 32 * hq + 32; c += 8) {
             float v8[8];
             umma::ld_x8(tq + TM_S + c, v8);
@@ -1128,7 +1154,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             for (int e = 0; e < 8; ++e) state[(size_t)(c + e) * DK + j] = v8[e];
         }
     }
-    if (LAYER && ok && tid < 3 * DK) {  // conv cache <- the last three inputs of (cache, x)
+    if (LAYER && all_ok && tid < 3 * DK) {  // conv cache <- the last three inputs of (cache, x)
         TQ *cache = static_cast<TQ *>(a.cache);
         const TQ *x = static_cast<const TQ *>(a.q);
         const int X = tid / DK, c = tid % DK;
@@ -1149,50 +1175,6 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     if (warp == 0) umma::tmem_dealloc(tb, TM_COLS);
 }
 
-// cuTensorMapEncodeTiled, looked up once through the runtime (no link
-// against the driver library)
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_tiled() {
-    static const EncodeTiledFn fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-// A map over a row-major tensor whose dims are listed innermost first
-// (dims[0] = 128 channels, contiguous); strides follow from the dims, box
-// dims as given, zero fill outside the tensor.
-cudaError_t make_map(CUtensorMap *map, const void *base, bool bf16, int rank, const uint64_t *dims,
-                     const uint32_t *box, bool swizzle) {
-    const EncodeTiledFn fn = encode_tiled();
-    if (!fn) return cudaErrorNotSupported;
-    const uint64_t esz = bf16 ? 2 : 4;
-    cuuint64_t gdim[5], gstr[4];
-    cuuint32_t bdim[5], estr[5];
-    uint64_t stride = esz;
-    for (int i = 0; i < rank; ++i) {
-        gdim[i] = dims[i];
-        bdim[i] = box[i];
-        estr[i] = 1;
-        if (i > 0) gstr[i - 1] = stride;
-        stride *= dims[i];
-    }
-    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          (cuuint32_t)rank, const_cast<void *>(base), gdim, gstr, bdim, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <typename TQ, bool LAYER>
 cudaError_t make_maps(const PrefillArgs &a, PrefillMaps *mp) {
     const bool bf16 = sizeof(TQ) == 2;
@@ -1207,15 +1189,15 @@ cudaError_t make_maps(const PrefillArgs &a, PrefillMaps *mp) {
     cudaError_t e = cudaSuccess;
     memset(mp, 0, sizeof(PrefillMaps));
     if (LAYER) {
-        e = make_map(&mp->v, a.q, bf16, 5, d5, box_row5, false);
-        if (e == cudaSuccess && bf16) e = make_map(&mp->q, a.q, true, 5, d5, box_half, true);
+        e = make_tensor_map(&mp->v, a.q, bf16, 5, d5, box_row5, false);
+        if (e == cudaSuccess && bf16) e = make_tensor_map(&mp->q, a.q, true, 5, d5, box_half, true);
     } else {
-        e = make_map(&mp->v, a.v, bf16, 4, d4, box_row4, false);
-        if (e == cudaSuccess && bf16) e = make_map(&mp->q, a.q, true, 4, d4, box_half4, true);
-        if (e == cudaSuccess && bf16) e = make_map(&mp->k, a.k, true, 4, d4, box_half4, true);
+        e = make_tensor_map(&mp->v, a.v, bf16, 4, d4, box_row4, false);
+        if (e == cudaSuccess && bf16) e = make_tensor_map(&mp->q, a.q, true, 4, d4, box_half4, true);
+        if (e == cudaSuccess && bf16) e = make_tensor_map(&mp->k, a.k, true, 4, d4, box_half4, true);
     }
-    if (e == cudaSuccess && bf16) e = make_map(&mp->alpha, a.alpha, false, 4, d4, box_al, true);
-    if (e == cudaSuccess) e = make_map(&mp->o, a.o, false, 4, d4, box_row4, false);
+    if (e == cudaSuccess && bf16) e = make_tensor_map(&mp->alpha, a.alpha, false, 4, d4, box_al, true);
+    if (e == cudaSuccess) e = make_tensor_map(&mp->o, a.o, false, 4, d4, box_row4, false);
     return e;
 }
 
@@ -1247,12 +1229,13 @@ cudaError_t launch_prefill_layer(const PrefillArgs &a, int x_dtype, cudaStream_t
     return launch_tc_typed<float, true, false>(a, stream);
 }
 
-cudaError_t take_prefill_error(unsigned int *code) {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(code, g_prefill_error, sizeof(unsigned int));
-    if (e != cudaSuccess) return e;
-    if (*code) e = cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(unsigned int));
-    return e;
+cudaError_t read_prefill_error(unsigned int *code) {
+    return cudaMemcpyFromSymbol(code, g_prefill_error, sizeof(unsigned int));
+}
+
+cudaError_t clear_prefill_error() {
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(unsigned int));
 }
 
 }  // namespace kda

@@ -7,8 +7,23 @@
 
 #include <cstdint>
 
+// Budget (clock cycles) of every wait on data or work in flight: about two
+// seconds at 2 GHz. A build may lower it (-DKDA_WAIT_BUDGET=...) so that
+// waits give up before legitimate copies land, to exercise the exit paths;
+// with -DKDA_WAIT_POLL the waits also poll (mbarrier.test_wait) instead of
+// letting the hardware suspend the thread, so they give up within the budget.
+#ifndef KDA_WAIT_BUDGET
+#define KDA_WAIT_BUDGET 4000000000LL
+#endif
+
 namespace kda {
 namespace ptx {
+
+constexpr long long kWaitBudget = KDA_WAIT_BUDGET;
+// Budget of the waits on a kernel's exit path, after a wait gave up: the
+// copies and tensor-core products it issued must land before the CTA's
+// shared and tensor memory are released. Not lowered by KDA_WAIT_BUDGET.
+constexpr long long kDrainBudget = 4000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -36,6 +51,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
+#ifdef KDA_WAIT_POLL
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -43,6 +67,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
@@ -151,6 +176,23 @@ __device__ __forceinline__ void launch_dependents() {
 // Barrier over `nthreads` threads (multiple of 32) using hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `nthreads` threads (multiple of 32) on hardware barrier `id`
+// that also reduces a predicate: every thread gets true only if every
+// participating thread passed true. A kernel uses it where a bounded wait
+// may have given up in some threads: all of them leave together.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // Signals arrival at hardware barrier `id` without waiting (the producer side

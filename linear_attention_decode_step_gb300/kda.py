@@ -24,7 +24,7 @@ __all__ = [
     "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "KDA_F32", "KDA_BF16",
     "KDA_DECODE_AUTO", "KDA_DECODE_CLUSTER", "KDA_DECODE_STREAM",
     "KDA_PREFILL_AUTO", "KDA_PREFILL_SIMT", "KDA_PREFILL_TC", "kda_chunk_prefill", "kda_chunk_prefill_config",
-    "KdaError", "lib", "library_path", "header_functions",
+    "KdaError", "lib", "load", "library_path", "header_functions",
     "kda_status_string", "kda_last_cuda_error", "kda_version",
     "kda_conv_step", "kda_decode_step", "kda_decode_step_config", "kda_device_error",
     "kda_decode_step_fused", "kda_decode_tokens", "kda_prefill_layer",
@@ -88,6 +88,16 @@ def header_functions() -> list[str]:
     return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Loads a build of the library from `path` with the C signatures of
+    every entry point declared (its own symbols: loaded RTLD_LOCAL)."""
+    L = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        f = getattr(L, name)
+        f.argtypes, f.restype = args, res
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """The loaded library. Raises if it has not been built."""
     global _lib
@@ -98,11 +108,7 @@ def lib() -> ctypes.CDLL:
                 raise RuntimeError(
                     "libkda_gb300.so is not built (expected at %s); run "
                     "linear_attention_decode_step_gb300.build.build()" % path)
-            L = ctypes.CDLL(path)
-            for name, (args, res) in _SIGNATURES.items():
-                f = getattr(L, name)
-                f.argtypes, f.restype = args, res
-            _lib = L
+            _lib = load(path)
     return _lib
 
 

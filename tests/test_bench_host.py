@@ -102,7 +102,9 @@ def test_prefill_summary_fractions():
     s = bench.prefill_summary(1.0, 4, 4096, 6778.3, 1946.6, "k")
     assert abs(s["gb_s"] - 1916796928 / 1e9 / 1e-3) < 1e-6
     assert abs(s["frac_of_measured_hbm"] - s["gb_s"] / 6778.3) < 1e-12
-    assert abs(s["tf32_peak_tflop_s"] - 1946.6 / 2) < 1e-12
+    # the TF32 peak: the measured BF16 peak times the nominal 1.1 / 2.25 PF ratio
+    assert abs(s["tf32_peak_tflop_s"] - 1946.6 * 1.1 / 2.25) < 1e-9
+    assert s["tf32_peak_kind"] == "measured bf16 x nominal 1.1/2.25"
     assert abs(s["tokens_per_s"] - 4 * 4096 / 1e-3) < 1e-3
 
 
@@ -133,3 +135,22 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     assert cb["sample"]
     assert line["config"]["M"] == 32 and line["config"]["layers"] == 34
+
+
+def test_traffic_only_for_the_measured_kernel_source(tmp_path, monkeypatch):
+    """The roofline's traffic comes from the committed measurement only while
+    the decode kernel's source is the one it was taken on, and only for the
+    M and state dtype it was taken at."""
+    import hashlib
+    import json
+    src = hashlib.sha256(open(bench.DECODE_SRC, "rb").read()).hexdigest()
+    data = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_DATA", str(data))
+    assert bench.ncu_traffic_per_launch(32, "f32") is None          # no file
+    rows = [{"M": 32, "state_dtype": "f32", "dram_bytes": 2.5e8}]
+    data.write_text(json.dumps({"kernel_source_sha256": src, "per_launch": rows}))
+    assert bench.ncu_traffic_per_launch(32, "f32") == 2.5e8
+    assert bench.ncu_traffic_per_launch(32, "bf16") is None
+    assert bench.ncu_traffic_per_launch(8, "f32") is None
+    data.write_text(json.dumps({"kernel_source_sha256": "0" * 64, "per_launch": rows}))
+    assert bench.ncu_traffic_per_launch(32, "f32") is None          # another source

@@ -10,8 +10,8 @@ import pytest
 
 import oracle
 from linear_attention_decode_step_gb300 import inputs
-from tests.kda_testlib import (TOL_BF16_STATE, TOL_F32_STATE, DeviceLayer, oracle_layer,
-                               rel_err, to_f64)
+from tests.kda_testlib import (TOL_BF16_STATE, TOL_F32_STATE, DeviceLayer, pool_map,
+                               oracle_layer, rel_err, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,8 +114,10 @@ def test_each_kernel_M32(K, kernel, state_dtype, x_dtype):
     streaming kernel, so every ring stage is reused), three steps."""
     inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, 100), M=32, T=3)
     dl = DeviceLayer(inp, state_dtype, x_dtype)
-    kern = K.KDA_DECODE_CLUSTER if kernel == "cluster" else K.KDA_DECODE_STREAM
-    outs = _run(K, dl, 3, kernel=kern) if kernel == "stream" else _run(K, dl, 3, tile=(32, 128))
+    if kernel == "cluster":
+        outs = _run(K, dl, 3, tile=(32, 128))
+    else:
+        outs = _run(K, dl, 3, kernel=K.KDA_DECODE_STREAM)
     ref, S, cache = oracle_layer(inp)
     _compare(dl, outs, ref, S, cache, _tol(state_dtype))
 
@@ -212,25 +214,54 @@ def test_zero_input_degenerate(K):
     _compare(dl, outs, ref, S, cache, TOL_F32_STATE)
 
 
+@pytest.mark.parametrize("M", [8, 32])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-def test_34_layer_stack_under_cuda_graph(K, state_dtype):
-    """34 independent layers, M=8, one token, launched as one captured CUDA
-    graph (the bench's launch configuration); every layer checked."""
-    L, M = 34, 8
-    layers = [DeviceLayer(inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, l), M=M, T=1), state_dtype)
-              for l in range(L)]
+def test_34_layer_stack_under_cuda_graph(K, state_dtype, M):
+    """34 independent layers launched as one captured CUDA graph per token,
+    exactly as the bench launches them (programmatic dependent launch between
+    layers, each layer's state prefetched into L2 before it waits for the
+    previous one), at M=8 and at the benchmarked M=32, for two tokens (two
+    replays, the state carried). Each token of every layer is checked against
+    one oracle step taken from the state the GPU had stored before it (with
+    BF16 storage that state is rounded, and the bar holds per step; two steps
+    against an unrounded reference would compound two roundings)."""
+    L, T = 34, 2
+    layers = [DeviceLayer(inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, l), M=M, T=T),
+                          state_dtype) for l in range(L)]
+    outs = [[torch.empty_like(dl.o) for _ in range(T)] for dl in layers]
     s = torch.cuda.Stream()
+    graphs = []
     with torch.cuda.stream(s):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for dl in layers:
-                K.kda_decode_step(dl.x[0], dl.conv_w, dl.cache, dl.alpha[0], dl.beta[0],
-                                  dl.state, dl.o)
-    g.replay()
+        for t in range(T):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for dl, ol in zip(layers, outs):
+                    K.kda_decode_step(dl.x[t], dl.conv_w, dl.cache, dl.alpha[t], dl.beta[t],
+                                      dl.state, ol[t])
+            graphs.append(g)
+    states = []  # the state each layer held before token t, as stored (host copies)
+    for t, g in enumerate(graphs):
+        torch.cuda.synchronize()
+        states.append([dl.state.cpu() for dl in layers])
+        g.replay()
     torch.cuda.synchronize()
-    for dl in layers:
-        ref, S, cache = oracle_layer(dl.inp)
-        _compare(dl, [dl.o.double().cpu().numpy()], ref, S, cache, _tol(state_dtype))
+    assert K.kda_device_error() == K.KDA_OK
+    tol = _tol(state_dtype)
+
+    def check(l):
+        dl, inp = layers[l], layers[l].inp
+        cache = inp["cache_f32"].astype(np.float64)
+        for t in range(T):
+            o_ref, S_ref, cache = oracle.decode_step(inp["x_f32"][t], inp["conv_w"], cache,
+                                                     inp["alpha"][t], inp["beta"][t],
+                                                     to_f64(states[t][l]))
+            e = rel_err(outs[l][t].double().cpu().numpy(), o_ref)
+            assert e <= tol, "layer %d token %d: o rel err %.3e" % (l, t, e)
+            got = to_f64(states[t + 1][l] if t + 1 < T else dl.state)
+            e = rel_err(got, S_ref)
+            assert e <= tol, "layer %d token %d: S rel err %.3e" % (l, t, e)
+        np.testing.assert_array_equal(to_f64(dl.cache), cache)
+    pool_map(check, list(range(L)))
 
 
 @pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
