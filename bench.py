@@ -609,6 +609,15 @@ def time_tokens(torch, kda, inputs, M, T, state_dtype, K, W):
     return e0.elapsed_time(e1) / K
 
 
+# Calls of at least this many tokens run the chunked multi-token kernel (the
+# library's dispatch rule in kda_decode_tokens.cu).
+TOKENS_WY_MIN = 4
+
+
+def tokens_kernel_name(T):
+    return "kda_decode_tokens_wy_kernel" if T >= TOKENS_WY_MIN else "kda_decode_tokens_kernel"
+
+
 def tokens_summary(ms, M, T, state_dtype, peak_hbm, sm_mhz):
     """Roofline of one multi-token call: the state is read and written once
     (HBM), each token costs 7 dk dv flops per head on CUDA cores (fade,
@@ -860,11 +869,14 @@ def own_arm(args, rank: int, world: int, local_rank: int):
     if not args.no_tokens:
         mhz = clk.get("sm_mhz") if isinstance(clk, dict) else None
         rows = [tokens_summary(time_tokens(torch, kda, inputs, M_, T, args.state_dtype, 30, 3),
-                               M_, T, args.state_dtype, peak, mhz) for T in (2, 4, 8)]
+                               M_, T, args.state_dtype, peak, mhz) for T in (2, 4, 8, 16)]
+        for r in rows:
+            r["kernel"] = tokens_kernel_name(r["T"])
         line["decode_tokens"] = {
             "workload": "multi-token decode (kda_decode_tokens): one layer, M=%d streams x 64 "
                         "heads, T tokens per call, %s state, BF16 q/k/v" % (M_, args.state_dtype),
-            "kernel": "kda_decode_tokens_kernel",
+            "kernel": "kda_decode_tokens_kernel (T < %d), kda_decode_tokens_wy_kernel (T >= %d)"
+                      % (TOKENS_WY_MIN, TOKENS_WY_MIN),
             "fp32_peak_tflop_s": fp32_peak_tflops(mhz),
             "fp32_peak_kind": "152 SMs x 128 FP32 lanes x 2 x SM clock (%s MHz)"
                               % ("sampled %.0f" % mhz if mhz else "max 2070"),

@@ -161,7 +161,11 @@ kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w
  *                               when stored at the end of the call.
  *   o           [M, T, H, dv]   FP32 outputs of every token
  *   T >= 1 (state traffic is amortised over T; the arithmetic grows with T,
- *   so for long inputs the chunked prefill is the faster path).
+ *   so for long inputs the chunked prefill is the faster path). Calls of 4
+ *   or more tokens regroup the recurrence into chunks of up to 8 tokens
+ *   (section 8.2.4's WY form, FP32 throughout): results agree with the
+ *   token-by-token order to FP32 rounding, and two calls split at a multiple
+ *   of 8 tokens reproduce one call bit for bit.
  * Other arguments, checks and errors as kda_decode_step (sizes scale with T).
  */
 kda_status kda_decode_tokens(const void *x, int x_dtype, const float *conv_w,

@@ -1,8 +1,13 @@
 // Multi-token KDA decode for sm_103a: T consecutive decode steps of one layer
 // in one launch (conv + SiLU, L2 norm of q and k, the gated delta rule of
 // "GLM-5.3 deep dive" section 8.2.3 Eq. 1 in the fade / predict / correct /
-// read order of section 8.2.6, readout o = w + d (k.q)), token after token,
-// as fla's fused-recurrent mode does for short inputs (section 8.2.5).
+// read order of section 8.2.6, readout o = w + d (k.q)). Two kernels: short
+// calls go token after token, as fla's fused-recurrent mode does for short
+// inputs (section 8.2.5); calls of KDA_TOKENS_WY_MIN tokens or more take the
+// same recurrence regrouped into chunks of up to 8 tokens (the WY
+// representation and UT transform of section 8.2.4, exact in FP32 on CUDA
+// cores), which passes over the state twice per chunk instead of four times
+// per token.
 //
 // Every mbarrier wait is bounded (about two seconds of clock cycles). A
 // thread whose wait gives up sets this file's device error word; the group's
@@ -19,6 +24,12 @@
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
 #include "kda_ptx.cuh"
+
+// Calls of at least this many tokens take the chunked kernel, shorter ones
+// the token-by-token kernel.
+#ifndef KDA_TOKENS_WY_MIN
+#define KDA_TOKENS_WY_MIN 4
+#endif
 
 namespace kda {
 
@@ -446,24 +457,576 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
     if (threadIdx.x == 0) drain_fills<C>(smem);
 }
 
+// ---------------------------------------------------------------------------
+// Chunked form for several tokens per head: the WY representation with the
+// UT transform of "GLM-5.3 deep dive" section 8.2.4, on CUDA cores in exact
+// FP32, for chunks of up to CT = 8 tokens. Within a chunk with state S0 at
+// its start, write R(t, j) = prod_{s = j+1 .. t} alpha_s (per key row; empty
+// product 1) and Gamma_t = R(t, -1). Then, with k and q L2-normalised,
+//   u_j   = (Gamma_j k_j) . S0 + sum_{i<j} A_ji d_i,  A_ji = sum_c k_jc k_ic R_c(j, i)
+//   d_j   = beta_j (v_j - u_j)                      (forward substitution)
+//   o_t   = scale ((Gamma_t q_t) . S0 + sum_{j<=t} P_tj d_j),  P_tj = sum_c q_tc k_jc R_c(t, j)
+//   S_end = Gamma_last S0 + sum_j (k_j R(last, j)) d_j^T
+// which is the token-by-token recurrence regrouped (no approximation). The
+// decay ratios are formed as products of alphas, never as quotients, so no
+// factor exceeds 1.
+//
+// Per chunk a group runs three phases:
+//  P1 (thread per channel): conv + SiLU of the chunk's q, k (one channel
+//     each) and v (one channel, half the tokens), alpha and beta into shared
+//     memory;                                                   group barrier
+//  P2 (warp t per token t): the norms of q_t, k_t, the rows A_t. and P_t. (raw,
+//     unnormalised), and Gamma_t q_t, Gamma_t k_t, k_t R(last, t), Gamma_last
+//     into row-permuted buffers;                                group barrier
+//  P3 (the state in registers, warp cw owning value columns 16 cw .. + 15 of
+//     all 128 key rows as in the token-by-token kernel): one pass forms the
+//     2 x CT column sums (Gamma k) . S0 and (Gamma q) . S0 and reduces them
+//     inside the warp; lanes holding u-side sums solve for d of their column,
+//     lanes holding q-side sums form o; a second pass applies the fade and
+//     the rank-CT update. No barrier: each warp owns its columns.
+// The norms are applied by the consumers: with rq, rk the inverse norms,
+// X_raw = (Gamma k_raw) . S0 and d'_j = rk_j d_j,
+//   d_j = beta_j (v_j - rk_j (X_raw_j + sum_{i<j} A_raw_ji d'_i)),
+//   o_t = scale rq_t (Y_raw_t + sum_{j<=t} P_raw_tj d'_j),
+//   S_end = Gamma_last S0 + sum_j (k_raw_j R(last, j)) d'_j^T.
+// ---------------------------------------------------------------------------
 template <typename TS, typename TX>
-cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream) {
-    constexpr int G = 2;
-    using C = TokCfg<TS, TX, G>;
-    auto kernel = kda_decode_tokens_kernel<TS, TX, G>;
+struct WyCfg {
+    static constexpr int G = 2;
+    static constexpr int CWARPS = kWarps / G;          // 8 warps, 16 value columns each
+    static constexpr int GT = CWARPS * 32;
+    static constexpr int THREADS = kWarps * 32;
+    static constexpr int CT = 8;                       // tokens per chunk: one per warp in P2
+    static_assert(CT == CWARPS && CWARPS * 16 == DK, "one warp per token, 16 columns per warp");
+    static constexpr int S_BYTES = DK * DK * (int)sizeof(TS);
+    static constexpr int C_OFF = S_BYTES;
+    static constexpr int STAGE = C_OFF + 9 * DK * (int)sizeof(TX);
+    // row-permuted vectors: lane group rl's 16 rows at 16 rl + 4 (rl / 2), so
+    // the 8 groups' 16-byte reads fall into 8 different bank quads
+    static constexpr int VP = 144;
+    // per group (floats): q | k conv outputs [CT][256] (channel order), alpha
+    // [CT][128], v [2][CT][128] and beta [2][CT] (by chunk parity: P3 of one
+    // chunk may still read them while P1 of the next writes), Gamma q, Gamma k,
+    // k R(last, .) [CT][VP], Gamma_last [VP], per token the P row, A row, rq,
+    // rk [CT][32], and per warp d' of its 16 columns [CWARPS][CT][16]
+    static constexpr int QK_F = 0;
+    static constexpr int AL_F = QK_F + CT * 2 * DK;
+    static constexpr int V_F = AL_F + CT * DK;
+    static constexpr int BT_F = V_F + 2 * CT * DK;
+    static constexpr int QD_F = BT_F + 2 * CT;
+    static constexpr int KD_F = QD_F + CT * VP;
+    static constexpr int KE_F = KD_F + CT * VP;
+    static constexpr int GL_F = KE_F + CT * VP;
+    static constexpr int RED_F = GL_F + VP;
+    static constexpr int DX_F = RED_F + CT * 32;
+    static constexpr int WORK_F = DX_F + CWARPS * CT * 16;
+    static constexpr int WORK_BYTES = WORK_F * 4;
+    static constexpr int BAR_BYTES = 2 * 8 * 8 + 8 * 4;  // full[8], issued[8], fills[8]
+    static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
+    static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
+    static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
+    static_assert(NST >= 2, "at least two stages must fit");
+    static_assert(QD_F % 4 == 0 && STAGE % 16 == 0 && WORK_BYTES % 16 == 0, "16-byte alignment");
+    static_assert(STAGE == TokCfg<TS, TX, G>::STAGE, "the stage layout of load_head_tokens");
+};
+
+__device__ __forceinline__ int wy_base(int rl) { return 16 * rl + 4 * (rl >> 1); }
+__device__ __forceinline__ int wy_pos(int i) { return wy_base(i & 7) + (i >> 3); }
+
+template <typename TX>
+__device__ __forceinline__ float conv4(const float4 w, TX a0, TX a1, TX a2, TX a3) {
+    const float pre = w.x * widen(a0) + w.y * widen(a1) + w.z * widen(a2) + w.w * widen(a3);
+    return __fdividef(pre, 1.0f + __expf(-pre));
+}
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+__device__ __forceinline__ float4 mul4(const float4 a, const float4 b) {
+    return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+
+// Sums v[0..15] over the 32 lanes of a warp; lane L returns the total of
+// v[(L >> 1) & 15] (halving exchanges, then one full one).
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+    constexpr unsigned F = 0xffffffffu;
+    float v8[8], v4[4], v2[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v8[i] = (b4 ? v[i + 8] : v[i]) + __shfl_xor_sync(F, b4 ? v[i] : v[i + 8], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v4[i] = (b3 ? v8[i + 4] : v8[i]) + __shfl_xor_sync(F, b3 ? v8[i] : v8[i + 4], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        v2[i] = (b2 ? v4[i + 2] : v4[i]) + __shfl_xor_sync(F, b2 ? v4[i] : v4[i + 2], 4);
+    const float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(F, b1 ? v2[0] : v2[1], 2);
+    return v1 + __shfl_xor_sync(F, v1, 1);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+template <typename TS, typename TX, bool MULTI>
+__global__ void __launch_bounds__(WyCfg<TS, TX>::THREADS, 1)
+kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
+    using C = WyCfg<TS, TX>;
+    constexpr int G = C::G, CT = C::CT, VP = C::VP;
+    constexpr bool kRowPairs = sizeof(TS) == 2;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
+    uint64_t *issued = full + 8;
+    volatile uint32_t *fills = reinterpret_cast<volatile uint32_t *>(issued + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H;
+    const int n_units = a.M * H;
+    const size_t D = (size_t)H * DK;
+    const uint64_t pol = ptx::policy_evict_first();
+
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&issued[s], 1);
+            fills[s] = blockIdx.x + s * gridDim.x < n_units ? 1u : 0u;
+        }
+        ptx::fence_mbar_init();
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units)
+                ptx::bulk_prefetch_l2(static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES);
+        }
+    }
+    __syncthreads();
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units) load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, u, pol);
+        }
+    }
+
+    const int g = warp / C::CWARPS;
+    const int ct = tid - g * C::GT;
+    const int cw = ct >> 5;
+    const int rl = lane >> 2, cc = lane & 3;
+    const int col0 = 16 * cw + 4 * cc;           // this lane's four value columns
+    const int lcol = 4 * cc + (rl & 3);           // the column (within the warp's 16) it ends with
+    const bool yside = lane & 16;                 // ends with q-side sums (else u-side)
+    const int rb = wy_base(rl);
+    const uint32_t bar_id = 1 + g;
+    float *buf = reinterpret_cast<float *>(smem + C::NST * C::STAGE + g * C::WORK_BYTES);
+    float *dxw = buf + C::DX_F + cw * CT * 16;
+    const TX *x = static_cast<const TX *>(a.x);
+    TX *cache = static_cast<TX *>(a.cache);
+    const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
+
+    // P1 channels: q (X = 0) or k (X = 1) channel ch for every token of a
+    // chunk, and v channel ch for half vh of the chunk's tokens
+    const int X = ct >> 7, ch = ct & (DK - 1), vh = ct >> 7;
+    // (T <= CT: one chunk, and the state is not live through P1 and P2)
+    const int nchunks = MULTI ? (T + CT - 1) / CT : 1;
+    const size_t xs = 3 * D;                      // token stride of x
+    int par = 0;
+    bool ok = true;
+
+    for (int i = g, u = blockIdx.x + g * gridDim.x; u < n_units; i += G, u += G * gridDim.x) {
+        const int s = i % C::NST, n = i / C::NST;
+        const int m = u / H, h = u - m * H;
+        const size_t hb = (size_t)h * DK;
+        const TS *Ss = reinterpret_cast<const TS *>(smem + s * C::STAGE);
+        const TX *cs = reinterpret_cast<const TX *>(smem + s * C::STAGE + C::C_OFF);
+        const TX *xqk = x + ((size_t)m * T * 3 + X) * D + hb + ch;
+        const TX *xvv = x + ((size_t)m * T * 3 + 2) * D + hb + ch;
+        // The lane's 64 state values as FP32 pairs. BF16 storage: sv[4 p + e] =
+        // rows rl + 16 p and rl + 16 p + 8 of column col0 + e (a natural pair of
+        // the row-permuted vectors, slots 2 p and 2 p + 1, so the column sums
+        // and the update need no broadcasts; unpacking places the values
+        // freely). FP32 storage: sv[2 r + k] = columns col0 + 2 k, + 1 of row
+        // rl + 8 r (whole row quads move between memory and registers).
+        float2 sv[32];
+
+        for (int c = 0; c < nchunks; ++c, par ^= 1) {
+            const int t0 = c * CT;
+            const int nc = min(CT, T - t0);
+            const bool last = c == nchunks - 1;
+            const int h0 = (nc + 1) >> 1;
+            const int vb = vh ? h0 : 0, vn = vh ? nc - h0 : h0;  // v tokens vb .. vb + vn - 1
+
+            // ---- P1: inputs (x of tokens t0 - 3 .. t0 + nc - 1 for the windows) ----
+            const float4 wq = __ldg(w4 + (size_t)X * D + hb + ch);
+            const float4 wv = __ldg(w4 + 2 * D + hb + ch);
+            TX xq[CT + 3], xv[CT / 2 + 3];
+            float av[CT / 2];
+#pragma unroll
+            for (int j = 0; j < CT + 3; ++j) {
+                const int tau = t0 - 3 + j;
+                xq[j] = (j < nc + 3 && tau >= 0) ? xqk[(size_t)tau * xs] : zero_tx<TX>();
+            }
+#pragma unroll
+            for (int j = 0; j < CT / 2 + 3; ++j) {
+                const int tau = t0 + vb - 3 + j;
+                xv[j] = (j < vn + 3 && tau >= 0) ? xvv[(size_t)tau * xs] : zero_tx<TX>();
+            }
+#pragma unroll
+            for (int j = 0; j < CT / 2; ++j)
+                av[j] = j < vn ? __ldg(a.alpha + ((size_t)(m * T + t0 + vb + j) * H + h) * DK + ch) : 0.f;
+            const float bt = ct < nc ? __ldg(a.beta + (size_t)(m * T + t0 + ct) * H + h) : 0.f;
+            // the conv cache after the call (inputs T - 3 .. T - 1), read here and
+            // written once the group barrier below has cleared the head
+            TX cq[3], cv[3];
+#pragma unroll
+            for (int e = 0; e < 3; ++e) {
+                const int tau = T - 3 + e;
+                cq[e] = (last && tau >= 0) ? xqk[(size_t)tau * xs] : zero_tx<TX>();
+                cv[e] = (last && vh && tau >= 0) ? xvv[(size_t)tau * xs] : zero_tx<TX>();
+            }
+            bool landed = true;
+            if (c == 0) {
+                // the stage's refill was issued, then its bytes landed; the
+                // window slots before token 0 come from its conv cache
+                landed = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                         ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+                if (!landed) raise_error(8u);
+#pragma unroll
+                for (int j = 0; j < 3; ++j) xq[j] = cs[(3 * X + j) * DK + ch];
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    if (vb - 3 + j < 0) xv[j] = cs[(6 + vb + j) * DK + ch];
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {  // slots of the cache still in the window (T < 3)
+                    const int tau = T - 3 + e;
+                    if (last && tau < 0) {
+                        cq[e] = cs[(3 * X + 3 + tau) * DK + ch];
+                        cv[e] = cs[(9 + tau) * DK + ch];
+                    }
+                }
+            }
+            float *qk = buf + C::QK_F, *al = buf + C::AL_F;
+            float *vbuf = buf + C::V_F + par * CT * DK, *bbuf = buf + C::BT_F + par * CT;
+#pragma unroll
+            for (int t = 0; t < CT; ++t)
+                if (t < nc) qk[t * 2 * DK + ct] = conv4(wq, xq[t], xq[t + 1], xq[t + 2], xq[t + 3]);
+#pragma unroll
+            for (int j = 0; j < CT / 2; ++j)
+                if (j < vn) {
+                    vbuf[(vb + j) * DK + ch] = conv4(wv, xv[j], xv[j + 1], xv[j + 2], xv[j + 3]);
+                    al[(vb + j) * DK + ch] = av[j];
+                }
+            if (ct < nc) bbuf[ct] = bt;
+
+            // every thread's wait succeeded (else the group leaves together,
+            // before anything of this head reaches global memory)
+            if (c == 0) {
+                if (!ptx::named_bar_and(bar_id, C::GT, landed)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                ptx::named_bar_sync(bar_id, C::GT);
+            }
+            if (last) {
+                const size_t cbase = (size_t)m * 9 * D + hb;
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    cache[cbase + (size_t)(3 * X + e) * D + ch] = cq[e];
+                    if (vh) cache[cbase + (size_t)(6 + e) * D + ch] = cv[e];
+                }
+            }
+
+            // ---- P2: warp t = cw takes token t ----
+            if (cw < nc) {
+                const int t = cw;
+                const float4 *qk4 = reinterpret_cast<const float4 *>(qk);
+                const float4 *al4 = reinterpret_cast<const float4 *>(al);
+                const float4 q4 = qk4[t * 64 + lane], k4 = qk4[t * 64 + 32 + lane];
+                float red[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) red[j] = 0.f;
+                const float qkd = dot4(q4, k4);
+#pragma unroll
+                for (int j = 0; j < CT; ++j)
+                    if (j == t) red[j] = qkd;
+                float4 R = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+                for (int j = CT - 2; j >= 0; --j)
+                    if (j < t) {
+                        R = mul4(R, al4[(j + 1) * 32 + lane]);
+                        const float4 kw = mul4(qk4[j * 64 + 32 + lane], R);
+                        red[j] = dot4(q4, kw);      // P_tj
+                        red[8 + j] = dot4(k4, kw);  // A_tj
+                    }
+                const float4 Gm = mul4(R, al4[lane]);  // Gamma_t
+                float4 E = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+                for (int j = 1; j < CT; ++j)
+                    if (j > t && j < nc) E = mul4(E, al4[j * 32 + lane]);
+                float *qd = buf + C::QD_F + t * VP, *kd = buf + C::KD_F + t * VP;
+                float *ke = buf + C::KE_F + t * VP, *gl = buf + C::GL_F;
+                const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+                const float gv[4] = {Gm.x, Gm.y, Gm.z, Gm.w}, ev[4] = {E.x, E.y, E.z, E.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int p = wy_pos(4 * lane + e);
+                    qd[p] = gv[e] * qv[e];
+                    kd[p] = gv[e] * kv[e];
+                    ke[p] = ev[e] * kv[e];
+                    if (t == nc - 1) gl[p] = gv[e];
+                }
+                const float tot = warp_sum16(red, lane);
+                const float qq = warp_sum(dot4(q4, q4)), kk = warp_sum(dot4(k4, k4));
+                float *rr = buf + C::RED_F + t * 32;
+                if ((lane & 1) == 0) rr[lane >> 1] = tot;
+                if (lane == 1) {
+                    rr[16] = rsqrtf(qq + kL2Eps);
+                    rr[17] = rsqrtf(kk + kL2Eps);
+                }
+            }
+            if (c == 0) {
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    if constexpr (kRowPairs) {
+                        float lo[4], hi[4];
+                        Quad<TS>::load(Ss + (rl + 16 * p) * DK + col0, lo);
+                        Quad<TS>::load(Ss + (rl + 16 * p + 8) * DK + col0, hi);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sv[4 * p + e] = make_float2(lo[e], hi[e]);
+                    } else {
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            float f4[4];
+                            Quad<TS>::load(Ss + (rl + 16 * p + 8 * h2) * DK + col0, f4);
+                            sv[2 * (2 * p + h2)] = make_float2(f4[0], f4[1]);
+                            sv[2 * (2 * p + h2) + 1] = make_float2(f4[2], f4[3]);
+                        }
+                    }
+                }
+            }
+            ptx::named_bar_sync(bar_id, C::GT);  // the chunk's vectors and rows are ready
+            if (c == 0 && ct == 0) {             // the stage is read: refill it
+                const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
+                if (ur < n_units) {
+                    load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                    fills[s] = fills[s] + 1u;
+                    ptx::mbar_arrive(&issued[s]);
+                }
+            }
+
+            // ---- P3, first pass: column sums of Gamma k and Gamma q over this lane's rows ----
+            // Per token, the lane's 2 x 4 sums reduce over the 8 lane groups rl in
+            // three halving exchanges: u / q side (lane bit 4), then column pairs
+            // (bit 3), then columns (bit 2). Lanes of the q side take the vectors in
+            // the other order, so the first exchange needs no select.
+            float xy[CT];
+            {
+                const float *own = buf + (yside ? C::QD_F : C::KD_F) + rb;
+                const float *oth = buf + (yside ? C::KD_F : C::QD_F) + rb;
+                const bool b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+                for (int t = 0; t < CT; ++t) {
+                    xy[t] = 0.f;
+                    if (t < nc) {
+                        float so[4], sx[4];  // own / other kind, per column
+                        if constexpr (kRowPairs) {
+                            float2 ao[4], ax[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) ao[e] = ax[e] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int r4 = 0; r4 < 4; ++r4) {
+                                const float4 fo = *reinterpret_cast<const float4 *>(own + t * VP + 4 * r4);
+                                const float4 fx = *reinterpret_cast<const float4 *>(oth + t * VP + 4 * r4);
+                                const float2 o0 = make_float2(fo.x, fo.y), o1 = make_float2(fo.z, fo.w);
+                                const float2 x0 = make_float2(fx.x, fx.y), x1 = make_float2(fx.z, fx.w);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    ao[e] = __ffma2_rn(o0, sv[8 * r4 + e], ao[e]);
+                                    ax[e] = __ffma2_rn(x0, sv[8 * r4 + e], ax[e]);
+                                    ao[e] = __ffma2_rn(o1, sv[8 * r4 + 4 + e], ao[e]);
+                                    ax[e] = __ffma2_rn(x1, sv[8 * r4 + 4 + e], ax[e]);
+                                }
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                so[e] = ao[e].x + ao[e].y;
+                                sx[e] = ax[e].x + ax[e].y;
+                            }
+                        } else {
+                            float2 ao[2], ax[2];
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) ao[k] = ax[k] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int r4 = 0; r4 < 4; ++r4) {
+                                const float4 fo = *reinterpret_cast<const float4 *>(own + t * VP + 4 * r4);
+                                const float4 fx = *reinterpret_cast<const float4 *>(oth + t * VP + 4 * r4);
+                                const float vo[4] = {fo.x, fo.y, fo.z, fo.w}, vx[4] = {fx.x, fx.y, fx.z, fx.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 wo = make_float2(vo[e], vo[e]), wx = make_float2(vx[e], vx[e]);
+#pragma unroll
+                                    for (int k = 0; k < 2; ++k) {
+                                        ao[k] = __ffma2_rn(wo, sv[2 * (4 * r4 + e) + k], ao[k]);
+                                        ax[k] = __ffma2_rn(wx, sv[2 * (4 * r4 + e) + k], ax[k]);
+                                    }
+                                }
+                            }
+                            so[0] = ao[0].x; so[1] = ao[0].y; so[2] = ao[1].x; so[3] = ao[1].y;
+                            sx[0] = ax[0].x; sx[1] = ax[0].y; sx[2] = ax[1].x; sx[3] = ax[1].y;
+                        }
+                        float l1[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) l1[e] = so[e] + __shfl_xor_sync(FULL, sx[e], 16);
+                        float l2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            l2[e] = (b3 ? l1[2 + e] : l1[e]) + __shfl_xor_sync(FULL, b3 ? l1[e] : l1[2 + e], 8);
+                        xy[t] = (b2 ? l2[1] : l2[0]) + __shfl_xor_sync(FULL, b2 ? l2[0] : l2[1], 4);
+                    }
+                }
+            }
+            const float *rrow = buf + C::RED_F;
+            if (!yside) {  // forward substitution for d' of column lcol
+                const float *vv = buf + C::V_F + par * CT * DK + 16 * cw + lcol;
+                const float4 *bb4 = reinterpret_cast<const float4 *>(buf + C::BT_F + par * CT);
+                const float4 ba = bb4[0], bz = bb4[1];
+                const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bz.x, bz.y, bz.z, bz.w};
+                float dp[CT];
+#pragma unroll
+                for (int j = 0; j < CT; ++j) {
+                    dp[j] = 0.f;
+                    if (j < nc) {
+                        const float4 *arow = reinterpret_cast<const float4 *>(rrow + j * 32 + 8);
+                        const float4 a0 = arow[0], a1 = arow[1];
+                        const float av8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        const float2 nrm = *reinterpret_cast<const float2 *>(rrow + j * 32 + 16);
+                        float acc = xy[j];
+#pragma unroll
+                        for (int i2 = 0; i2 < j; ++i2) acc += av8[i2] * dp[i2];
+                        dp[j] = nrm.y * (bv[j] * (vv[j * DK] - nrm.y * acc));
+                        dxw[j * 16 + lcol] = dp[j];
+                    }
+                }
+            }
+            __syncwarp();
+            if (yside) {  // outputs of column lcol
+                float dp[CT];
+#pragma unroll
+                for (int j = 0; j < CT; ++j) dp[j] = j < nc ? dxw[j * 16 + lcol] : 0.f;
+                float *op = a.o + ((size_t)(m * T + t0) * H + h) * DK + 16 * cw + lcol;
+#pragma unroll
+                for (int t = 0; t < CT; ++t)
+                    if (t < nc) {
+                        const float4 *prow = reinterpret_cast<const float4 *>(rrow + t * 32);
+                        const float4 p0 = prow[0], p1 = prow[1];
+                        const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                        float acc = xy[t];
+#pragma unroll
+                        for (int j = 0; j <= t; ++j) acc += pv[j] * dp[j];
+                        op[(size_t)t * H * DK] = a.scale * rrow[t * 32 + 16] * acc;
+                    }
+            }
+
+            // ---- P3, second pass: fade by Gamma_last, then the rank-nc update ----
+            {
+                const float *glv = buf + C::GL_F + rb, *kev = buf + C::KE_F + rb;
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(glv + 4 * r4);
+                    if constexpr (kRowPairs) {
+                        const float2 g0 = make_float2(g4.x, g4.y), g1 = make_float2(g4.z, g4.w);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            sv[8 * r4 + e] = __fmul2_rn(sv[8 * r4 + e], g0);
+                            sv[8 * r4 + 4 + e] = __fmul2_rn(sv[8 * r4 + 4 + e], g1);
+                        }
+                    } else {
+                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 g2 = make_float2(gv[e], gv[e]);
+                            sv[2 * (4 * r4 + e)] = __fmul2_rn(sv[2 * (4 * r4 + e)], g2);
+                            sv[2 * (4 * r4 + e) + 1] = __fmul2_rn(sv[2 * (4 * r4 + e) + 1], g2);
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (int j = 0; j < nc; ++j) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dxw + j * 16 + 4 * cc);
+                    if constexpr (kRowPairs) {
+                        const float2 dd[4] = {make_float2(d4.x, d4.x), make_float2(d4.y, d4.y),
+                                              make_float2(d4.z, d4.z), make_float2(d4.w, d4.w)};
+#pragma unroll
+                        for (int r4 = 0; r4 < 4; ++r4) {
+                            const float4 e4 = *reinterpret_cast<const float4 *>(kev + j * VP + 4 * r4);
+                            const float2 e0 = make_float2(e4.x, e4.y), e1 = make_float2(e4.z, e4.w);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                sv[8 * r4 + e] = __ffma2_rn(e0, dd[e], sv[8 * r4 + e]);
+                                sv[8 * r4 + 4 + e] = __ffma2_rn(e1, dd[e], sv[8 * r4 + 4 + e]);
+                            }
+                        }
+                    } else {
+                        const float2 dd[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
+#pragma unroll
+                        for (int r4 = 0; r4 < 4; ++r4) {
+                            const float4 e4 = *reinterpret_cast<const float4 *>(kev + j * VP + 4 * r4);
+                            const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 e2 = make_float2(ev[e], ev[e]);
+                                sv[2 * (4 * r4 + e)] = __ffma2_rn(e2, dd[0], sv[2 * (4 * r4 + e)]);
+                                sv[2 * (4 * r4 + e) + 1] = __ffma2_rn(e2, dd[1], sv[2 * (4 * r4 + e) + 1]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (!ok) break;
+
+        // state out (rounded once, here, for BF16 storage)
+        TS *Sg = static_cast<TS *>(a.state) + (size_t)u * DK * DK + col0;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float f4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f4[e] = kRowPairs ? (h2 ? sv[4 * p + e].y : sv[4 * p + e].x)
+                                      : (e & 1 ? sv[2 * (2 * p + h2) + (e >> 1)].y
+                                               : sv[2 * (2 * p + h2) + (e >> 1)].x);
+                Quad<TS>::store(Sg + (size_t)(rl + 16 * p + 8 * h2) * DK, f4);
+            }
+        }
+    }
+
+    // Exit: as in the token-by-token kernel
+    __syncthreads();
+    if (threadIdx.x == 0) drain_fills<C>(smem);
+}
+
+template <typename KERNEL>
+cudaError_t launch_persistent(KERNEL kernel, int threads, int smem, const DecodeArgs &a, int T,
+                              cudaStream_t stream) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int units = a.M * a.H;
     const int grid = units < sms ? units : sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -471,6 +1034,20 @@ cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, a, T);
+}
+
+template <typename TS, typename TX>
+cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream) {
+    if (T >= KDA_TOKENS_WY_MIN) {
+        using C = WyCfg<TS, TX>;
+        if (T > C::CT)
+            return launch_persistent(kda_decode_tokens_wy_kernel<TS, TX, true>, C::THREADS, C::SMEM, a, T,
+                                     stream);
+        return launch_persistent(kda_decode_tokens_wy_kernel<TS, TX, false>, C::THREADS, C::SMEM, a, T,
+                                 stream);
+    }
+    using C = TokCfg<TS, TX, 2>;
+    return launch_persistent(kda_decode_tokens_kernel<TS, TX, 2>, C::THREADS, C::SMEM, a, T, stream);
 }
 
 }  // namespace

@@ -68,9 +68,12 @@ def test_decode_step_times_out_then_library_is_usable(libs, state_dtype):
     assert rel_err(dl.o.double().cpu().numpy(), ref[0]) <= tol
 
 
-def test_decode_tokens_times_out_then_library_is_usable(libs):
+@pytest.mark.parametrize("T", [2, 4, 12])
+def test_decode_tokens_times_out_then_library_is_usable(libs, T):
+    """T = 2 runs the token-by-token kernel, 4 the chunked kernel with one
+    chunk, 12 the chunked kernel with two."""
     kda, short = libs
-    inp = inputs.decode_layer(8200, M=8, T=4)
+    inp = inputs.decode_layer(8200, M=8, T=T)
     tok = inputs.stack_tokens(inp)
     dev = "cuda"
 
@@ -78,10 +81,10 @@ def test_decode_tokens_times_out_then_library_is_usable(libs):
         return (bits_to_torch_bf16(tok["x_bits"], dev), torch.from_numpy(inp["conv_w"]).to(dev),
                 bits_to_torch_bf16(inp["cache_bits"], dev), torch.from_numpy(tok["alpha"]).to(dev),
                 torch.from_numpy(tok["beta"]).to(dev), torch.from_numpy(inp["S0"]).to(dev).clone(),
-                torch.empty((8, 4, 64, 128), dtype=torch.float32, device=dev))
+                torch.empty((8, T, 64, 128), dtype=torch.float32, device=dev))
     x, w, cache, alpha, beta, S, o = bufs()
     st = short.kda_decode_tokens(_p(x), kda.KDA_BF16, _p(w), _p(cache), kda.KDA_BF16, _p(alpha),
-                                 _p(beta), _p(S), kda.KDA_F32, 1.0, _p(o), 8, 4, 64, 128, 128, None)
+                                 _p(beta), _p(S), kda.KDA_F32, 1.0, _p(o), 8, T, 64, 128, 128, None)
     assert st == kda.KDA_OK
     assert short.kda_device_error(None) == kda.KDA_ERR_TIMEOUT
     x, w, cache, alpha, beta, S, o = bufs()
