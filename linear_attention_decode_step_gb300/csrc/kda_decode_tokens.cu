@@ -474,7 +474,9 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 // Per chunk a group runs three phases:
 //  P1 (thread per channel): conv + SiLU of the chunk's q, k (one channel
 //     each) and v (one channel, half the tokens), alpha and beta into shared
-//     memory;                                                   group barrier
+//     memory (with FP32 state and BF16 inputs, x and alpha of the chunk were
+//     copied into shared memory by bulk copies the group's first warp issued
+//     one chunk earlier, on a per-group mbarrier);              group barrier
 //  P2 (warp t per token t): the norms of q_t, k_t, the rows A_t. and P_t. (raw,
 //     unnormalised), and Gamma_t q_t, Gamma_t k_t, k_t R(last, t), Gamma_last
 //     into row-permuted buffers;                                group barrier
@@ -501,15 +503,22 @@ struct WyCfg {
     static constexpr int S_BYTES = DK * DK * (int)sizeof(TS);
     static constexpr int C_OFF = S_BYTES;
     static constexpr int STAGE = C_OFF + 9 * DK * (int)sizeof(TX);
+    // With FP32 state and BF16 inputs, the next chunk's inputs are staged in
+    // shared memory by bulk copies issued a chunk ahead (FP32 inputs would need
+    // twice the room; with BF16 state the direct loads measured faster)
+    static constexpr bool kStageX = sizeof(TX) == 2 && sizeof(TS) == 4;
     // row-permuted vectors: lane group rl's 16 rows at 16 rl + 4 (rl / 2), so
     // the 8 groups' 16-byte reads fall into 8 different bank quads
     static constexpr int VP = 144;
-    // per group (floats): q | k conv outputs [CT][256] (channel order), alpha
-    // [CT][128], v [2][CT][128] and beta [2][CT] (by chunk parity: P3 of one
-    // chunk may still read them while P1 of the next writes), Gamma q, Gamma k,
-    // k R(last, .) [CT][VP], Gamma_last [VP], per token the P row, A row, rq,
-    // rk [CT][32], and per warp d' of its 16 columns [CWARPS][CT][16]
+    // per group (floats): q | k conv outputs [CT][256] (channel order; during
+    // P3 a warp keeps d' of its 16 columns in its own 32-float slots of each
+    // row, which only its own threads write in P1), alpha [CT][128], v
+    // [2][CT][128] and beta [2][CT] (by chunk parity: P3 of one chunk may still
+    // read them while P1 of the next writes), Gamma q, Gamma k, k R(last, .)
+    // [CT][VP], Gamma_last [VP], per token the P row, A row, rq, rk [CT][32],
+    // and with staged inputs x of tokens t0 - 3 .. t0 + CT - 1 [3][CT + 3][128]
     static constexpr int QK_F = 0;
+    static constexpr int DXS = 2 * DK;             // row stride of the d' slots
     static constexpr int AL_F = QK_F + CT * 2 * DK;
     static constexpr int V_F = AL_F + CT * DK;
     static constexpr int BT_F = V_F + 2 * CT * DK;
@@ -518,15 +527,19 @@ struct WyCfg {
     static constexpr int KE_F = KD_F + CT * VP;
     static constexpr int GL_F = KE_F + CT * VP;
     static constexpr int RED_F = GL_F + VP;
-    static constexpr int DX_F = RED_F + CT * 32;
-    static constexpr int WORK_F = DX_F + CWARPS * CT * 16;
+    static constexpr int XS_F = RED_F + CT * 32;
+    static constexpr int XS_BYTES = kStageX ? 3 * (CT + 3) * DK * (int)sizeof(TX) : 0;
+    static constexpr int WORK_F = XS_F + XS_BYTES / 4;
     static constexpr int WORK_BYTES = WORK_F * 4;
-    static constexpr int BAR_BYTES = 2 * 8 * 8 + 8 * 4;  // full[8], issued[8], fills[8]
+    // full[8], issued[8], fills[8], then the input barriers xin[2] and their
+    // fill counts [2]
+    static constexpr int BAR_BYTES = 2 * 8 * 8 + 8 * 4 + 2 * 8 + 2 * 4 + 8;
     static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
     static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
     static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
     static_assert(NST >= 2, "at least two stages must fit");
-    static_assert(QD_F % 4 == 0 && STAGE % 16 == 0 && WORK_BYTES % 16 == 0, "16-byte alignment");
+    static_assert(QD_F % 4 == 0 && XS_F % 4 == 0 && STAGE % 16 == 0 && WORK_BYTES % 16 == 0,
+                  "16-byte alignment");
     static_assert(STAGE == TokCfg<TS, TX, G>::STAGE, "the stage layout of load_head_tokens");
 };
 
@@ -582,6 +595,9 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
     uint64_t *issued = full + 8;
     volatile uint32_t *fills = reinterpret_cast<volatile uint32_t *>(issued + 8);
+    // staged inputs: per group an mbarrier and the number of fills issued into it
+    uint64_t *xin = full + 20;
+    volatile uint32_t *xfills = reinterpret_cast<volatile uint32_t *>(full + 22);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
@@ -594,6 +610,10 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&issued[s], 1);
             fills[s] = blockIdx.x + s * gridDim.x < n_units ? 1u : 0u;
+        }
+        for (int gg = 0; gg < G; ++gg) {
+            ptx::mbar_init(&xin[gg], 1);
+            xfills[gg] = 0u;
         }
         ptx::fence_mbar_init();
         for (int s = 0; s < C::NST; ++s) {
@@ -622,7 +642,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
     const int rb = wy_base(rl);
     const uint32_t bar_id = 1 + g;
     float *buf = reinterpret_cast<float *>(smem + C::NST * C::STAGE + g * C::WORK_BYTES);
-    float *dxw = buf + C::DX_F + cw * CT * 16;
+    float *dxw = buf + C::QK_F + 32 * cw;       // d' of this warp's columns, row stride DXS
     const TX *x = static_cast<const TX *>(a.x);
     TX *cache = static_cast<TX *>(a.cache);
     const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
@@ -635,6 +655,40 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
     const size_t xs = 3 * D;                      // token stride of x
     int par = 0;
     bool ok = true;
+
+    // Staged inputs of unit (uu, cn) (head uu, chunk cn): x of tokens
+    // t0 - 3 .. t0 + nc - 1 (from t0 for the first chunk, whose window starts in
+    // the conv cache) into [X][slot = token - t0 + 3], alpha of the chunk's
+    // tokens into the alpha buffer; completes on this group's input barrier.
+    const TX *xsm = reinterpret_cast<const TX *>(buf + C::XS_F);
+    uint32_t xk = 0;  // inputs consumed by this group
+    // Issued by the 32 lanes of the group's first warp, one or two copies each.
+    auto stage_inputs = [&](int uu, int cn) {
+        const int mm = uu / H, hh = uu - mm * H;
+        const int tt0 = cn * CT, ncn = min(CT, T - tt0);
+        const int first = cn == 0 ? tt0 : tt0 - 3, ntok = tt0 + ncn - first;
+        if (lane == 0)
+            ptx::mbar_arrive_expect_tx(&xin[g], 3u * (uint32_t)ntok * DK * sizeof(TX) +
+                                                    (uint32_t)ncn * DK * 4u);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            int j = lane + 32 * r;
+            if (j < 3 * ntok) {
+                const int X2 = j / ntok, tau = first + j - X2 * ntok;
+                ptx::bulk_g2s(reinterpret_cast<unsigned char *>(buf + C::XS_F) +
+                                  (size_t)(X2 * (CT + 3) + tau - tt0 + 3) * DK * sizeof(TX),
+                              x + ((size_t)(mm * T + tau) * 3 + X2) * D + (size_t)hh * DK,
+                              DK * sizeof(TX), &xin[g]);
+            } else if ((j -= 3 * ntok) < ncn) {
+                ptx::bulk_g2s(buf + C::AL_F + j * DK,
+                              a.alpha + ((size_t)(mm * T + tt0 + j) * H + hh) * DK, DK * 4, &xin[g]);
+            }
+        }
+        if (lane == 0) xfills[g] = xfills[g] + 1u;
+    };
+    if (C::kStageX && cw == 0 && blockIdx.x + g * gridDim.x < n_units)
+        stage_inputs(blockIdx.x + g * gridDim.x, 0);
 
     for (int i = g, u = blockIdx.x + g * gridDim.x; u < n_units; i += G, u += G * gridDim.x) {
         const int s = i % C::NST, n = i / C::NST;
@@ -664,36 +718,57 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
             const float4 wv = __ldg(w4 + 2 * D + hb + ch);
             TX xq[CT + 3], xv[CT / 2 + 3];
             float av[CT / 2];
-#pragma unroll
-            for (int j = 0; j < CT + 3; ++j) {
-                const int tau = t0 - 3 + j;
-                xq[j] = (j < nc + 3 && tau >= 0) ? xqk[(size_t)tau * xs] : zero_tx<TX>();
-            }
-#pragma unroll
-            for (int j = 0; j < CT / 2 + 3; ++j) {
-                const int tau = t0 + vb - 3 + j;
-                xv[j] = (j < vn + 3 && tau >= 0) ? xvv[(size_t)tau * xs] : zero_tx<TX>();
-            }
-#pragma unroll
-            for (int j = 0; j < CT / 2; ++j)
-                av[j] = j < vn ? __ldg(a.alpha + ((size_t)(m * T + t0 + vb + j) * H + h) * DK + ch) : 0.f;
-            const float bt = ct < nc ? __ldg(a.beta + (size_t)(m * T + t0 + ct) * H + h) : 0.f;
-            // the conv cache after the call (inputs T - 3 .. T - 1), read here and
-            // written once the group barrier below has cleared the head
-            TX cq[3], cv[3];
-#pragma unroll
-            for (int e = 0; e < 3; ++e) {
-                const int tau = T - 3 + e;
-                cq[e] = (last && tau >= 0) ? xqk[(size_t)tau * xs] : zero_tx<TX>();
-                cv[e] = (last && vh && tau >= 0) ? xvv[(size_t)tau * xs] : zero_tx<TX>();
-            }
+            TX cq[3], cv[3];  // the conv cache after the call: inputs T - 3 .. T - 1
             bool landed = true;
-            if (c == 0) {
-                // the stage's refill was issued, then its bytes landed; the
-                // window slots before token 0 come from its conv cache
-                landed = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
-                         ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+            const float bt = ct < nc ? __ldg(a.beta + (size_t)(m * T + t0 + ct) * H + h) : 0.f;
+            if constexpr (C::kStageX) {
+                // this chunk's inputs landed (issued a chunk ahead)
+                landed = ptx::mbar_wait(&xin[g], xk & 1, ptx::kWaitBudget);
+                ++xk;
+                if (c == 0)  // the stage's refill was issued, then its bytes landed
+                    landed = landed &&
+                             (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                             ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
                 if (!landed) raise_error(8u);
+#pragma unroll
+                for (int j = 0; j < CT + 3; ++j)
+                    xq[j] = j < nc + 3 ? xsm[(X * (CT + 3) + j) * DK + ch] : zero_tx<TX>();
+#pragma unroll
+                for (int j = 0; j < CT / 2 + 3; ++j)
+                    xv[j] = j < vn + 3 ? xsm[(2 * (CT + 3) + vb + j) * DK + ch] : zero_tx<TX>();
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    cq[e] = last ? xsm[(X * (CT + 3) + nc + e) * DK + ch] : zero_tx<TX>();
+                    cv[e] = last ? xsm[(2 * (CT + 3) + nc + e) * DK + ch] : zero_tx<TX>();
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < CT + 3; ++j) {
+                    const int tau = t0 - 3 + j;
+                    xq[j] = (j < nc + 3 && tau >= 0) ? xqk[(size_t)tau * xs] : zero_tx<TX>();
+                }
+#pragma unroll
+                for (int j = 0; j < CT / 2 + 3; ++j) {
+                    const int tau = t0 + vb - 3 + j;
+                    xv[j] = (j < vn + 3 && tau >= 0) ? xvv[(size_t)tau * xs] : zero_tx<TX>();
+                }
+#pragma unroll
+                for (int j = 0; j < CT / 2; ++j)
+                    av[j] = j < vn ? __ldg(a.alpha + ((size_t)(m * T + t0 + vb + j) * H + h) * DK + ch) : 0.f;
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    const int tau = T - 3 + e;
+                    cq[e] = (last && tau >= 0) ? xqk[(size_t)tau * xs] : zero_tx<TX>();
+                    cv[e] = (last && vh && tau >= 0) ? xvv[(size_t)tau * xs] : zero_tx<TX>();
+                }
+                if (c == 0) {
+                    // the stage's refill was issued, then its bytes landed
+                    landed = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                             ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+                    if (!landed) raise_error(8u);
+                }
+            }
+            if (c == 0) {  // the window slots before token 0 come from the stage's conv cache
 #pragma unroll
                 for (int j = 0; j < 3; ++j) xq[j] = cs[(3 * X + j) * DK + ch];
 #pragma unroll
@@ -717,13 +792,13 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
             for (int j = 0; j < CT / 2; ++j)
                 if (j < vn) {
                     vbuf[(vb + j) * DK + ch] = conv4(wv, xv[j], xv[j + 1], xv[j + 2], xv[j + 3]);
-                    al[(vb + j) * DK + ch] = av[j];
+                    if (!C::kStageX) al[(vb + j) * DK + ch] = av[j];
                 }
             if (ct < nc) bbuf[ct] = bt;
 
-            // every thread's wait succeeded (else the group leaves together,
-            // before anything of this head reaches global memory)
-            if (c == 0) {
+            // every thread's wait succeeded (else the group leaves together, before
+            // anything of this chunk reaches global memory)
+            if (c == 0 || C::kStageX) {
                 if (!ptx::named_bar_and(bar_id, C::GT, landed)) {
                     ok = false;
                     break;
@@ -809,6 +884,11 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
                 }
             }
             ptx::named_bar_sync(bar_id, C::GT);  // the chunk's vectors and rows are ready
+            if (C::kStageX && cw == 0) {  // the staged inputs are read: stage the next chunk's
+                const bool more = c + 1 < nchunks;
+                const int un = more ? u : u + G * gridDim.x;
+                if (un < n_units) stage_inputs(un, more ? c + 1 : 0);
+            }
             if (c == 0 && ct == 0) {             // the stage is read: refill it
                 const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
                 if (ur < n_units) {
@@ -908,7 +988,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
 #pragma unroll
                         for (int i2 = 0; i2 < j; ++i2) acc += av8[i2] * dp[i2];
                         dp[j] = nrm.y * (bv[j] * (vv[j * DK] - nrm.y * acc));
-                        dxw[j * 16 + lcol] = dp[j];
+                        dxw[j * C::DXS + lcol] = dp[j];
                     }
                 }
             }
@@ -916,7 +996,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
             if (yside) {  // outputs of column lcol
                 float dp[CT];
 #pragma unroll
-                for (int j = 0; j < CT; ++j) dp[j] = j < nc ? dxw[j * 16 + lcol] : 0.f;
+                for (int j = 0; j < CT; ++j) dp[j] = j < nc ? dxw[j * C::DXS + lcol] : 0.f;
                 float *op = a.o + ((size_t)(m * T + t0) * H + h) * DK + 16 * cw + lcol;
 #pragma unroll
                 for (int t = 0; t < CT; ++t)
@@ -956,7 +1036,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
                 }
 #pragma unroll 1
                 for (int j = 0; j < nc; ++j) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dxw + j * 16 + 4 * cc);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dxw + j * C::DXS + 4 * cc);
                     if constexpr (kRowPairs) {
                         const float2 dd[4] = {make_float2(d4.x, d4.x), make_float2(d4.y, d4.y),
                                               make_float2(d4.z, d4.z), make_float2(d4.w, d4.w)};
@@ -1006,9 +1086,16 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
         }
     }
 
-    // Exit: as in the token-by-token kernel
+    // Exit: as in the token-by-token kernel, and the latest staged inputs of
+    // each group (in flight only if the group left early)
     __syncthreads();
-    if (threadIdx.x == 0) drain_fills<C>(smem);
+    if (threadIdx.x == 0) {
+        drain_fills<C>(smem);
+        for (int gg = 0; gg < G; ++gg) {
+            const uint32_t f = xfills[gg];
+            if (f > 0) ptx::mbar_wait(&xin[gg], (f - 1) & 1, ptx::kDrainBudget);
+        }
+    }
 }
 
 template <typename KERNEL>
