@@ -306,7 +306,8 @@ __device__ __forceinline__ void fetch_qka(QKA<__nv_bfloat16> &R, const unsigned 
     }
 }
 template <typename TQ, bool LAYER, bool NORM>
-__global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ PrefillMaps mp) {
+__global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ PrefillMaps mp,
+                                                                const int item_base, const int piece_chunks) {
     // BF16 q, k arrive by tensor copies into shared memory; FP32 ones (twice
     // the bytes: no room to stage) by register loads a chunk ahead
     constexpr bool kTma = sizeof(TQ) == 2;
@@ -328,7 +329,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     float4 *sWqk = reinterpret_cast<float4 *>(sm + S_WQK);
     float *sBias = reinterpret_cast<float *>(sm + S_BIAS);
 
-    const int h = blockIdx.x % a.H, m = blockIdx.x / a.H;
+    // work item: piece `piece` (chunks piece * piece_chunks .. + piece_chunks - 1)
+    // of sequence (m, h); a launch holds pieces whose predecessors an earlier
+    // launch on the stream has finished (the state passes between them in place)
+    const int item = item_base + (int)blockIdx.x;
+    const int seq = item % (a.M * a.H), piece = item / (a.M * a.H);
+    const int h = seq % a.H, m = seq / a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // token-channel mapping
     const int cg = warp & 7, rh = warp >> 3, rr = lane & 7, qq = lane >> 3;
@@ -338,6 +344,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     const int q4 = warp & 3, hq = warp >> 2;
     const int j = 32 * q4 + lane;                  // value channel (TMEM lane)
     const int T = a.T;
+    const int t_begin = piece * piece_chunks * C;
+    const int t_end = min(T, t_begin + piece_chunks * C);
     const uint32_t sbase = ptx::smem_u32(sm);
     if (sbase & 1023u) {  // the swizzled boxes need a 1024-byte aligned base
         if (tid == 0) raise_error(kPrefillErrMisaligned);
@@ -357,46 +365,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     umma::fence_after_sync();
     const uint32_t tb = *slot;
     const uint32_t tq = tb + ((uint32_t)(32 * q4) << 16);  // this warp's TMEM lane quarter
-
-    // state in: S^T[j][i] = S[i][j]; this thread: lane j, key channels [32 hq, 32 hq + 32)
-    float *state = a.state + ((size_t)m * a.H + h) * DK * DK;
-    for (int c = 32 * hq; c < 32 * hq + 32; c += 8) {
-        float v8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v8[e] = state[(size_t)(c + e) * DK + j];
-        umma::st_x8(tq + TM_S + c, v8);
-    }
-    umma::wait_st();
-
-    using RW = Raw<TQ>;
-    QKA<TQ> R;
-    float beta_n = 0.f;
-    if (!kTma) load_qka<TQ, LAYER>(R, a, m, h, r0, c4);
-    if (tid < C) beta_n = tid < T ? __ldg(a.beta + ((size_t)m * T + tid) * a.H + h) : 0.f;
-
-    // the layer form: gate constants, conv weights, the cache as the tokens
-    // before the first chunk, and the raw q, k before the second half
-    const size_t D = (size_t)a.H * DK;
-    if (LAYER) {
-        const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
-        if (tid < 3 * DK) sWqk[tid] = __ldg(w4 + (size_t)(tid >> 7) * D + (size_t)h * DK + (tid & 127));
-        if (tid < DK) sBias[tid] = __ldg(a.dt_bias + (size_t)h * DK + tid);
-        const TQ *cache = static_cast<const TQ *>(a.cache);
-        for (int i = tid; i < 3 * 3 * DK; i += NT) {  // xb[1][X][tap][c] (q, k) and vc[1][tap][c] (v) = cache
-            const int X = i / (3 * DK), tap = (i / DK) % 3, c = i % DK;
-            const float v = RW::widen1(RW::load1(cache + ((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c));
-            if (X < 2) sXb[XB_F + i] = v;
-            else sVc[3 * DK + tap * DK + c] = v;
-        }
-        if (!kTma && rh == 0 && rr >= 5) {  // tokens 29-31 of chunk 0 (lanes rr = 5, 6, 7 of g = 3)
-            float xq[4], xk[4];
-            RW::widen4(R.q[3], xq);
-            RW::widen4(R.k[3], xk);
-            *reinterpret_cast<float4 *>(sXa + (0 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xq[0], xq[1], xq[2], xq[3]);
-            *reinterpret_cast<float4 *>(sXa + (1 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xk[0], xk[1], xk[2], xk[3]);
-        }
-        __syncthreads();
-    }
+    // Launched with programmatic stream serialisation: the set-up above overlaps
+    // the previous grid's tail (the previous round's pieces, or whatever ran
+    // before); every global read comes after this wait, and the next grid may
+    // start placing its CTAs as SMs free up.
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
 
     // v of the chunk starting at token t0 -> sV (token-major [64][128], rows
     // past T zero), one tensor copy completing on bar[4]; thread kLoader
@@ -421,9 +395,57 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
 #pragma unroll
         for (int b = 0; b < 4; ++b) ptx::tma_load_4d(sm + ST_AL + b * BOX, &mp.alpha, &bar[5], 32 * b, h, t0, m);
     };
-    if (tid == kLoader) {
-        if (kTma) issue_qka(0);
-        issue_v(0);
+    if (tid == kLoader) {  // the first chunk's inputs, under the state copy below
+        if (kTma) issue_qka(t_begin);
+        issue_v(t_begin);
+    }
+
+
+    // state in: S^T[j][i] = S[i][j]; this thread: lane j, key channels [32 hq, 32 hq + 32)
+    float *state = a.state + ((size_t)m * a.H + h) * DK * DK;
+    for (int c = 32 * hq; c < 32 * hq + 32; c += 8) {
+        float v8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v8[e] = state[(size_t)(c + e) * DK + j];
+        umma::st_x8(tq + TM_S + c, v8);
+    }
+    umma::wait_st();
+
+    using RW = Raw<TQ>;
+    QKA<TQ> R;
+    float beta_n = 0.f;
+    if (!kTma) load_qka<TQ, LAYER>(R, a, m, h, t_begin + r0, c4);
+    if (tid < C) beta_n = t_begin + tid < T ? __ldg(a.beta + ((size_t)m * T + t_begin + tid) * a.H + h) : 0.f;
+
+    // the layer form: gate constants, conv weights, the cache as the tokens
+    // before the first chunk, and the raw q, k before the second half
+    const size_t D = (size_t)a.H * DK;
+    if (LAYER) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
+        if (tid < 3 * DK) sWqk[tid] = __ldg(w4 + (size_t)(tid >> 7) * D + (size_t)h * DK + (tid & 127));
+        if (tid < DK) sBias[tid] = __ldg(a.dt_bias + (size_t)h * DK + tid);
+        const TQ *cache = static_cast<const TQ *>(a.cache);
+        const TQ *xg = static_cast<const TQ *>(a.q);
+        // the three inputs before the piece's first chunk (the conv cache before
+        // token 0, else x) -> the buffers that chunk reads: xb[p][X][tap][c] (q, k)
+        // and vc[p][tap][c] (v), p = parity of the chunk before it
+        const int pb = ((t_begin / C) + 1) & 1;
+        for (int i = tid; i < 3 * 3 * DK; i += NT) {
+            const int X = i / (3 * DK), tap = (i / DK) % 3, c = i % DK;
+            const int t = t_begin - 3 + tap;
+            const float v = RW::widen1(t < 0 ? RW::load1(cache + ((size_t)m * 9 + 3 * X + tap) * D + (size_t)h * DK + c)
+                                             : RW::load1(xg + (((size_t)m * T + t) * 3 + X) * D + (size_t)h * DK + c));
+            if (X < 2) sXb[pb * XB_F + i] = v;
+            else sVc[pb * 3 * DK + tap * DK + c] = v;
+        }
+        if (!kTma && rh == 0 && rr >= 5) {  // tokens 29-31 of chunk 0 (lanes rr = 5, 6, 7 of g = 3)
+            float xq[4], xk[4];
+            RW::widen4(R.q[3], xq);
+            RW::widen4(R.k[3], xk);
+            *reinterpret_cast<float4 *>(sXa + (0 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xq[0], xq[1], xq[2], xq[3]);
+            *reinterpret_cast<float4 *>(sXa + (1 * 3 + rr - 5) * DK + 4 * c4) = make_float4(xk[0], xk[1], xk[2], xk[3]);
+        }
+        __syncthreads();
     }
 
     const uint32_t id128 = umma::instr_desc(128, 128, umma::kFmtTF32);
@@ -440,7 +462,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
     int last_bar = -1, last_par = 0;
     int phase = 0;
 
-    for (int c0 = 0; c0 < T; c0 += C, phase ^= 1) {
+    for (int c0 = t_begin; c0 < t_end; c0 += C, phase ^= 1) {
         // ---------------------------------------------------------- 1. decay, norms
         if constexpr (kTma) {
             if (!ptx::mbar_wait(&bar[5], phase, ptx::kWaitBudget)) {
@@ -688,7 +710,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         umma::fence_before_sync();
         // the previous chunk's O staging (over Kdec^T, rewritten while MMA1 runs)
         // has been read by its tensor store before anyone passes this barrier
-        if (tid == 0 && c0 > 0) ptx::bulk_wait_read_all();
+        if (tid == 0 && c0 > t_begin) ptx::bulk_wait_read_all();
         ptx::named_bar_sync(kBarMma1, NT);
         if (tid == kIssuer) {
             umma::fence_after_sync();
@@ -798,7 +820,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
         }
         // the next chunk's q, k, alpha (the registers of this one are consumed);
         // issued after the proxy fence above, which would otherwise wait for them
-        if (!kTma && c0 + C < T) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
+        if (!kTma && c0 + C < t_end) load_qka<TQ, LAYER>(R, a, m, h, c0 + C + r0, c4);
 
         // ---------------------------------------------------------- 5. M = (I + A)^-1 Diag(beta)
         // (warps 0-7, on CUDA cores, while MMA3 runs on the tensor cores and
@@ -962,7 +984,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             }
             umma::fence_after_sync();
             // MMA3 has read [Kd; Qd]: the region takes the next chunk's q, k, alpha
-            if (kTma && tid == kLoader && c0 + C < T && ok) {
+            if (kTma && tid == kLoader && c0 + C < t_end && ok) {
                 issue_qka(c0 + C);
                 ++qka_issued;
             }
@@ -1031,7 +1053,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             umma::wait_st();
         }
         // the layer form: raw q, k of tokens 29-31 of the next chunk (loaded in phase 4)
-        if (!kTma && LAYER && rh == 0 && rr >= 5 && c0 + C < T) {
+        if (!kTma && LAYER && rh == 0 && rr >= 5 && c0 + C < t_end) {
             float xq[4], xk[4];
             RW::widen4(R.q[3], xq);
             RW::widen4(R.k[3], xk);
@@ -1045,7 +1067,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             break;
         }
         umma::fence_after_sync();
-        if (tid == kLoader && c0 + C < T) {
+        if (tid == kLoader && c0 + C < t_end) {
             issue_v(c0 + C);
             ++v_issued;
         }
@@ -1154,7 +1176,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_tc_kernel(const PrefillArgs
             for (int e = 0; e < 8; ++e) state[(size_t)(c + e) * DK + j] = v8[e];
         }
     }
-    if (LAYER && all_ok && tid < 3 * DK) {  // conv cache <- the last three inputs of (cache, x)
+    if (LAYER && all_ok && t_end == T && tid < 3 * DK) {  // conv cache <- the last three inputs of (cache, x)
         TQ *cache = static_cast<TQ *>(a.cache);
         const TQ *x = static_cast<const TQ *>(a.q);
         const int X = tid / DK, c = tid % DK;
@@ -1201,6 +1223,35 @@ cudaError_t make_maps(const PrefillArgs &a, PrefillMaps *mp) {
     return e;
 }
 
+// Pieces per sequence. One CTA per SM walks one sequence's chunks one after
+// another, so with more sequences than SMs the launch runs in waves and the
+// last wave can leave SMs idle (256 sequences on 152 SMs: two waves, the
+// second on 104 SMs). Cutting each sequence into P pieces of consecutive
+// chunks and running the pieces in rounds of at most one per SM (piece p of
+// every sequence before piece p + 1; the state passes from piece to piece in
+// place, through the state buffer) balances the rounds. The cost model
+// counts chunk steps on the busiest SM plus about 0.8 of a chunk per round
+// (measured: the round boundary, state out and in, the first chunk's copies
+// not yet overlapped). P = 1 whenever
+// sequences do not outnumber SMs, so that every round holds at most one
+// piece of a sequence.
+int prefill_pieces(int sequences, int chunks, int sms) {
+    if (sequences < sms || chunks < 2) return 1;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int p = 1; p <= 8 && p <= chunks; ++p) {
+        const int per = (chunks + p - 1) / p;          // chunks per piece
+        const int pieces = (chunks + per - 1) / per;   // pieces per sequence
+        const int rounds = (sequences * pieces + sms - 1) / sms;
+        const double cost = (double)rounds * per + 0.8 * rounds;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = pieces;
+        }
+    }
+    return best;
+}
+
 template <typename TQ, bool LAYER, bool NORM>
 cudaError_t launch_tc_typed(const PrefillArgs &a, cudaStream_t stream) {
     PrefillMaps mp;
@@ -1209,8 +1260,34 @@ cudaError_t launch_tc_typed(const PrefillArgs &a, cudaStream_t stream) {
     auto kernel = kda_prefill_tc_kernel<TQ, LAYER, NORM>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kernel<<<dim3(a.M * a.H), NT, SMEM_BYTES, stream>>>(a, mp);
-    return cudaGetLastError();
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int seqs = a.M * a.H, chunks = (a.T + C - 1) / C;
+    const int pieces = prefill_pieces(seqs, chunks, sms);
+    const int per = (chunks + pieces - 1) / pieces;
+    const int items = seqs * ((chunks + per - 1) / per);
+    // one launch per round of at most `sms` pieces when cut, else one launch
+    // of one CTA per sequence
+    const int round = pieces > 1 ? sms : items;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    for (int base = 0; base < items; base += round) {
+        const int n = items - base < round ? items - base : round;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n, 1, 1);
+        cfg.blockDim = dim3(NT, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, a, mp, base, per);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace

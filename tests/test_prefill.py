@@ -210,3 +210,24 @@ def test_output_rows_past_T_untouched(K):
     assert bool(torch.all(pad[:, 70:] == 12345.0))
     o_ref, _ = _oracle(p)
     assert rel_err(o.double().cpu().numpy(), o_ref) <= TOL
+
+
+@pytest.mark.parametrize("qkv", ["bf16", "f32"])
+def test_pieces_equal_whole_sequences(K, qkv):
+    """M = 3 streams x 64 heads (192 sequences, more than the SMs) of 1000
+    tokens: the launcher cuts each sequence into pieces of consecutive chunks
+    and runs them in rounds, the state passing between pieces in place. Each
+    stream's outputs and final state equal, bit for bit, a call of that stream
+    alone (64 sequences, fewer than the SMs: one piece each), since a piece
+    boundary only stores and reloads the exact FP32 state."""
+    p = inputs.prefill_problem(8700, M=3, T=1000, H=64)
+    q, k, v, alpha, beta, S = _device(p, qkv)
+    o = K.kda_chunk_prefill(q, k, v, alpha, beta, S)
+    for m in range(3):
+        sl = lambda t: t[m:m + 1].contiguous()
+        S1 = sl(torch.from_numpy(p["S0"]).to("cuda"))
+        o1 = K.kda_chunk_prefill(sl(q), sl(k), sl(v), sl(alpha), sl(beta), S1)
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], o[m]), m
+        assert torch.equal(S1[0], S[m]), m
+    assert K.kda_device_error() == K.KDA_OK

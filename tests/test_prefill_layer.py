@@ -136,3 +136,19 @@ def test_layer_odd_shapes(K, M, T, H):
     assert rel_err(y, y_ref) <= TOL, rel_err(y, y_ref)
     assert rel_err(S, S_ref) <= TOL, rel_err(S, S_ref)
     np.testing.assert_array_equal(c, c_ref)
+
+
+def test_layer_pieces_equal_whole_sequences(K):
+    """The layer form at M = 3 x 64 heads x 1000 tokens (pieces in rounds, as
+    in test_prefill.py): each stream equals a call of that stream alone bit for
+    bit, outputs, final state and conv cache (a later piece takes its conv
+    window from x, the first from the cache; only the last writes the cache)."""
+    p = inputs.prefill_layer_problem(8710, M=3, T=1000, H=64)
+    y, S, cache = _run(K, p)
+    for m in range(3):
+        per_stream = ("x_bits", "x_f32", "cache_bits", "cache_f32", "f", "beta", "S0", "out_gate")
+        one = {n: (v[m:m + 1].copy() if n in per_stream else v) for n, v in p.items()}
+        y1, S1, c1 = _run(K, one)
+        np.testing.assert_array_equal(y1[0], y[m])
+        np.testing.assert_array_equal(S1[0], S[m])
+        np.testing.assert_array_equal(c1[0], cache[m])
