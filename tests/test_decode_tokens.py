@@ -163,3 +163,17 @@ def test_tokens_split_at_chunk_boundary_is_exact(K):
     assert torch.equal(o2, o)
     assert torch.equal(S2, S)
     assert torch.equal(cache, cache2)
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_tokens_extreme_decay(K, state_dtype):
+    """Decays from 1e-30 to exactly 1, mixed per channel and token, over two
+    chunks of the chunked kernel (T = 12): its decay ratios are products of
+    alphas (never quotients), so nothing overflows; outputs and state match
+    the oracle to the usual bar."""
+    def extreme(inp, tok):
+        rng = np.random.default_rng(9100)
+        choices = np.array([1e-30, 1e-3, 0.5, 0.999, 1.0], dtype=np.float32)
+        tok["alpha"] = choices[rng.integers(0, len(choices), size=tok["alpha"].shape)]
+    o, _, _ = _check(K, 2, 8, 12, state_dtype, seed=90, edit=extreme)
+    assert np.all(np.isfinite(o))
