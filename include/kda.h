@@ -189,8 +189,10 @@ typedef enum {
  * columns are split into slices of `columns` (16, 32, 64 or 128), one CTA of
  * `threads` threads each. With KDA_DECODE_STREAM, `columns` is the number of
  * heads (0-16) whose state is prefetched into L2 ahead of the shared-memory
- * ring and `threads` the number of consumer groups per CTA (1 or 2; 0 picks
- * the default).
+ * ring and `threads` the number of consumer groups per CTA (1 or 2, or 4
+ * with BF16 state: four groups of four warps holding the state packed; 0
+ * picks the default: 2 for FP32 state, 4 for BF16). With `threads` = 4 the
+ * L2 prefetch count is ignored.
  * Unsupported combinations return KDA_ERR_UNSUPPORTED. Same arguments,
  * layouts and results as kda_decode_step.
  */

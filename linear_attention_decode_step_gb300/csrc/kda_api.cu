@@ -163,7 +163,8 @@ kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_
     a.H = H;
     a.scale = scale;
     a.l2_prefetch = kda::kDefaultL2Prefetch;
-    int groups = kda::kDefaultGroups;
+    // BF16 state: four groups of four warps with the state packed in registers
+    int groups = state_dtype == KDA_BF16 ? kda::kDefaultGroupsBf16 : kda::kDefaultGroups;
     if (explicit_kernel && kernel == KDA_DECODE_STREAM) {
         if (columns < 0 || columns > 16) return KDA_ERR_UNSUPPORTED;
         a.l2_prefetch = columns;

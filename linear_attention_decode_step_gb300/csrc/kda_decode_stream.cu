@@ -526,6 +526,279 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// BF16 state, four consumer groups of four warps (launch_decode_stream with
+// groups = 4). Same ring protocol, stage layout and arithmetic as the kernel
+// above; what differs is the work split, for more heads in flight per SM:
+//  * A group is 128 threads, one per channel: thread ct convolves q, k and v
+//    channel ct and later forms d and o of value column ct, so a column's d
+//    and o come from one thread.
+//  * A thread holds 16 rows x 8 columns of the head's state packed as BF16
+//    (64 registers) and widens them twice, once for the column sums and once
+//    for the update (the state is rounded to BF16 exactly once, at the store,
+//    as above).
+//  * The fade is folded into the column sums (u = (alpha k).s, w = (alpha q).s)
+//    and into the update (S' = alpha s + k (rk d)), so no faded copy is kept.
+//  * Per row the conv thread publishes (alpha k, alpha q) for the column sums
+//    and (alpha, k) for the update, 8 bytes each.
+// ---------------------------------------------------------------------------
+template <typename TX>
+struct PCfg {
+    using TS = __nv_bfloat16;
+    using SC = Cfg<TS, TX, 2>;                   // the stage layout of load_head
+    static constexpr int G = 4;
+    static constexpr int CWARPS = kWarps / G;    // 4
+    static constexpr int GT = CWARPS * 32;       // 128: one thread per channel
+    static constexpr int THREADS = kWarps * 32;
+    static constexpr int VEC = 8;                // BF16 columns per 16-byte strip
+    static constexpr int STRIPS = DK / VEC;      // 16
+    static constexpr int SUBS = 32 / STRIPS;     // 2 rows per warp instruction
+    static constexpr int RGROUPS = CWARPS * SUBS;
+    static constexpr int RPT = DK / RGROUPS;     // 16 rows per thread
+    static_assert(GT == DK, "one thread per channel");
+    static constexpr int STAGE = SC::STAGE;
+    static constexpr int A_OFF = SC::A_OFF, X_OFF = SC::X_OFF, C_OFF = SC::C_OFF;
+    // per group (floats): red_u, red_w [CWARPS][DK] | d [DK] | v [2][DK] |
+    // per row (alpha k, alpha q) [DK][2] and (alpha, k) [DK][2], twice | norm
+    // partials [CWARPS][4]. v and the row entries alternate by the group's head
+    // parity: the update of one head still reads them after the last barrier
+    // while faster threads write the next head's.
+    static constexpr int REDW_F = CWARPS * DK;
+    static constexpr int DB_F = 2 * CWARPS * DK;
+    static constexpr int V_F = DB_F + DK;
+    static constexpr int ROW_F = V_F + 2 * DK;
+    static constexpr int NRM_F = ROW_F + 8 * DK;
+    static constexpr int WORK_F = NRM_F + 4 * CWARPS;
+    static constexpr int WORK_BYTES = WORK_F * 4;
+    static constexpr int BAR_BYTES = 2 * 8 * 8 + 8 * 4;  // full[8], issued[8], fills[8]
+    static constexpr int NST_FIT = (kSmemLimit - BAR_BYTES - G * WORK_BYTES) / STAGE;
+    // a multiple of G, so every stage serves one group only: with four groups
+    // and a stage shared between groups, a group running far enough ahead
+    // could see a parity two phases old (tests/test_ring_protocol.py models it)
+    static constexpr int NST = (NST_FIT > 8 ? 8 : NST_FIT) / G * G;
+    static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
+    static_assert(NST >= G, "a stage per group at least");
+    static_assert(STAGE % 16 == 0 && WORK_BYTES % 16 == 0, "16-byte alignment");
+};
+
+template <typename TX>
+__global__ void __launch_bounds__(PCfg<TX>::THREADS, 1)
+kda_decode_packed_kernel(const DecodeArgs a) {
+    using C = PCfg<TX>;
+    using TS = __nv_bfloat16;
+    constexpr int G = C::G;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
+    uint64_t *issued = full + 8;
+    volatile uint32_t *fills = reinterpret_cast<volatile uint32_t *>(issued + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H;
+    const int n_units = a.M * H;
+    const size_t D = (size_t)H * DK;
+    const uint64_t pol = ptx::policy_evict_first();
+
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&issued[s], 1);
+            fills[s] = blockIdx.x + s * gridDim.x < n_units ? 1u : 0u;
+        }
+        ptx::fence_mbar_init();
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units) prefetch_head<TS>(a, u);
+        }
+    }
+    __syncthreads();
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const int u = blockIdx.x + s * gridDim.x;
+            if (u < n_units) load_head<TS, TX, 2, false>(smem + s * C::STAGE, &full[s], a, u, pol);
+        }
+    }
+
+    const int g = warp / C::CWARPS;
+    const int ct = tid - g * C::GT;              // channel / value column of this thread
+    const int cwarp = ct >> 5;
+    const int strip = lane % C::STRIPS, sub = lane / C::STRIPS;
+    const int rg = cwarp * C::SUBS + sub;        // rows rg + RGROUPS p
+    const uint32_t bar_id = 1 + g;
+    float *red = reinterpret_cast<float *>(smem + C::NST * C::STAGE + g * C::WORK_BYTES);
+    float *redw = red + C::REDW_F;
+    float *db = red + C::DB_F;
+    float *vb = red + C::V_F;
+    float *rowd = red + C::ROW_F;
+    float *nrm = red + C::NRM_F;
+    TX *cache = static_cast<TX *>(a.cache);
+    const float4 *w4 = reinterpret_cast<const float4 *>(a.conv_w);
+
+    for (int i = g, u = blockIdx.x + g * gridDim.x; u < n_units; i += G, u += G * gridDim.x) {
+        const int s = i % C::NST, n = i / C::NST;
+        const int m = u / H, h = u - m * H;
+        const size_t hb = (size_t)h * DK;
+        const float4 wq = __ldg(w4 + hb + ct), wk = __ldg(w4 + D + hb + ct), wv = __ldg(w4 + 2 * D + hb + ct);
+        const float beta = __ldg(a.beta + u);
+        const int hp = (i / G) & 1;  // this head's v and row-entry buffers
+        float *vbh = vb + hp * DK, *rowh = rowd + hp * 4 * DK;
+
+        // the stage's refill was issued, then its bytes landed (a thread whose
+        // wait gives up reads no further data and writes nothing; the group
+        // leaves together at barrier 1)
+        const bool landed = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                            ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+        if (!landed) raise_error(4u);
+        const unsigned char *st = smem + s * C::STAGE;
+        const TS *Ss = reinterpret_cast<const TS *>(st);
+        const float *al = reinterpret_cast<const float *>(st + C::A_OFF);
+        const TX *xs = reinterpret_cast<const TX *>(st + C::X_OFF);
+        const TX *cs = reinterpret_cast<const TX *>(st + C::C_OFF);
+
+        // (a) this thread's 16 x 8 state values, packed
+        uint4 sp[C::RPT];
+#pragma unroll
+        for (int p = 0; p < C::RPT; ++p)
+            sp[p] = *reinterpret_cast<const uint4 *>(Ss + (p * C::RGROUPS + rg) * DK + strip * C::VEC);
+
+        // (b) conv + SiLU of channel ct of q, k and v; the row entry of key
+        // channel ct; warp partials of k.k, q.q, q.k
+        const size_t cbase = (size_t)m * 9 * D + hb;
+        float qv = 0.f, kv = 0.f, vv = 0.f;
+        if (landed) {
+            qv = conv_stage(wq, cs, xs, 0, ct, cache + cbase + ct, D);
+            kv = conv_stage(wk, cs, xs, 1, ct, cache + cbase + 3 * D + ct, D);
+            vv = conv_stage(wv, cs, xs, 2, ct, cache + cbase + 6 * D + ct, D);
+        }
+        const float ar = al[ct];
+        *reinterpret_cast<float2 *>(rowh + 2 * ct) = make_float2(ar * kv, ar * qv);
+        *reinterpret_cast<float2 *>(rowh + 2 * DK + 2 * ct) = make_float2(ar, kv);
+        vbh[ct] = vv;
+        float nk = kv * kv, nq = qv * qv, nb = qv * kv;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            nk += __shfl_xor_sync(0xffffffffu, nk, off);
+            nq += __shfl_xor_sync(0xffffffffu, nq, off);
+            nb += __shfl_xor_sync(0xffffffffu, nb, off);
+        }
+        if (lane == 0) {
+            nrm[4 * cwarp] = nk;
+            nrm[4 * cwarp + 1] = nq;
+            nrm[4 * cwarp + 2] = nb;
+        }
+        // barrier 1: stage read; rows, v, norm partials visible; every wait succeeded
+        if (!ptx::named_bar_and(bar_id, C::GT, landed)) break;
+        if (ct == 0) {
+            const int ur = blockIdx.x + (i + C::NST) * gridDim.x;  // refill with head i + NST
+            if (ur < n_units) {
+                load_head<TS, TX, 2, false>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                fills[s] = fills[s] + 1u;
+                ptx::mbar_arrive(&issued[s]);
+            }
+        }
+        float sk = 0.f, sq = 0.f, sb = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::CWARPS; ++w) {
+            sk += nrm[4 * w];
+            sq += nrm[4 * w + 1];
+            sb += nrm[4 * w + 2];
+        }
+        const float rk = 1.0f / sqrtf(sk + kL2Eps), rq = 1.0f / sqrtf(sq + kL2Eps);
+
+        // (c) column sums u = (alpha k).s and w = (alpha q).s over this thread's rows
+        float2 u2[4], w2[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u2[c] = w2[c] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < C::RPT; ++p) {
+            const float2 rw = *reinterpret_cast<const float2 *>(rowh + 2 * (p * C::RGROUPS + rg));
+            float f[8];
+            Strip<TS>::unpack(sp[p], f);
+            const float2 ka = make_float2(rw.x, rw.x), qa = make_float2(rw.y, rw.y);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 s2 = make_float2(f[2 * c], f[2 * c + 1]);
+                u2[c] = __ffma2_rn(ka, s2, u2[c]);
+                w2[c] = __ffma2_rn(qa, s2, w2[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // the warp's two row groups
+            u2[c].x += __shfl_xor_sync(0xffffffffu, u2[c].x, 16);
+            u2[c].y += __shfl_xor_sync(0xffffffffu, u2[c].y, 16);
+            w2[c].x += __shfl_xor_sync(0xffffffffu, w2[c].x, 16);
+            w2[c].y += __shfl_xor_sync(0xffffffffu, w2[c].y, 16);
+        }
+        if (sub == 0) {
+            float4 *ru = reinterpret_cast<float4 *>(red + cwarp * DK + strip * C::VEC);
+            float4 *rw4 = reinterpret_cast<float4 *>(redw + cwarp * DK + strip * C::VEC);
+            ru[0] = make_float4(u2[0].x, u2[0].y, u2[1].x, u2[1].y);
+            ru[1] = make_float4(u2[2].x, u2[2].y, u2[3].x, u2[3].y);
+            rw4[0] = make_float4(w2[0].x, w2[0].y, w2[1].x, w2[1].y);
+            rw4[1] = make_float4(w2[2].x, w2[2].y, w2[3].x, w2[3].y);
+        }
+        ptx::named_bar_sync(bar_id, C::GT);  // barrier 2: partial column sums
+
+        // (d) column ct: d = beta (v - u) (published as rk d) and o
+        {
+            float ut = 0.f, wt = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::CWARPS; ++w) {
+                ut += red[w * DK + ct];
+                wt += redw[w * DK + ct];
+            }
+            const float dj = rk * (beta * (vbh[ct] - rk * ut));
+            db[ct] = dj;
+            a.o[(size_t)u * DK + ct] = a.scale * rq * fmaf(dj, sb, wt);
+        }
+        ptx::named_bar_sync(bar_id, C::GT);  // barrier 3: d published
+
+        // (e) S' = alpha s + k (rk d), rounded once to BF16, streamed out
+        float dd[8];
+        {
+            const float4 d0 = reinterpret_cast<const float4 *>(db + strip * C::VEC)[0];
+            const float4 d1 = reinterpret_cast<const float4 *>(db + strip * C::VEC)[1];
+            dd[0] = d0.x; dd[1] = d0.y; dd[2] = d0.z; dd[3] = d0.w;
+            dd[4] = d1.x; dd[5] = d1.y; dd[6] = d1.z; dd[7] = d1.w;
+        }
+        TS *Sg = static_cast<TS *>(a.state) + (size_t)u * DK * DK + strip * C::VEC;
+#pragma unroll
+        for (int p = 0; p < C::RPT; ++p) {
+            const int row = p * C::RGROUPS + rg;
+            const float2 rw = *reinterpret_cast<const float2 *>(rowh + 2 * DK + 2 * row);
+            // widened again here rather than kept from the column sums (an opaque
+            // copy of the packed words, so the compiler does not keep 128 widened
+            // values live across the barriers instead)
+            uint4 pk;
+            asm volatile("mov.b32 %0, %4;\n\tmov.b32 %1, %5;\n\tmov.b32 %2, %6;\n\tmov.b32 %3, %7;"
+                         : "=r"(pk.x), "=r"(pk.y), "=r"(pk.z), "=r"(pk.w)
+                         : "r"(sp[p].x), "r"(sp[p].y), "r"(sp[p].z), "r"(sp[p].w));
+            float f[8], nv[8];
+            Strip<TS>::unpack(pk, f);
+            const float2 a2 = make_float2(rw.x, rw.x), k2 = make_float2(rw.y, rw.y);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 s2 = __fmul2_rn(a2, make_float2(f[2 * c], f[2 * c + 1]));
+                const float2 n2 = __ffma2_rn(k2, make_float2(dd[2 * c], dd[2 * c + 1]), s2);
+                nv[2 * c] = n2.x;
+                nv[2 * c + 1] = n2.y;
+            }
+            __stcs(reinterpret_cast<uint4 *>(Sg + (size_t)row * DK), Strip<TS>::pack(nv));
+        }
+    }
+
+    // Exit, as above: once all groups are here no thread issues another bulk
+    // copy; the latest fill of every stage has landed before the CTA goes.
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < C::NST; ++s) {
+            const uint32_t f = fills[s];
+            if (f > 0) ptx::mbar_wait(&full[s], (f - 1) & 1, ptx::kDrainBudget);
+        }
+    }
+}
+
 template <typename TS, typename TX, int G, bool GATE, bool NORM>
 cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
     using C = Cfg<TS, TX, G>;
@@ -552,10 +825,39 @@ cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+template <typename TX>
+cudaError_t launch_packed_typed(const DecodeArgs &a, cudaStream_t stream) {
+    using C = PCfg<TX>;
+    auto kernel = kda_decode_packed_kernel<TX>;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    const int units = a.M * a.H;
+    const int grid = units < sms ? units : sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <typename TS, typename TX>
 cudaError_t launch_groups(const DecodeArgs &a, int groups, cudaStream_t stream) {
     if (groups == 1) return launch_stream_typed<TS, TX, 1, false, false>(a, stream);
     if (groups == 2) return launch_stream_typed<TS, TX, 2, false, false>(a, stream);
+    if constexpr (sizeof(TS) == 2) {
+        if (groups == 4) return launch_packed_typed<TX>(a, stream);
+    }
     return cudaErrorNotSupported;
 }
 

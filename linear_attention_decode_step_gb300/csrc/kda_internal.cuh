@@ -11,7 +11,8 @@ namespace kda {
 
 constexpr int kHeadDim = 128;  // dk = dv handled by the decode and prefill kernels
 constexpr int kDefaultL2Prefetch = 0;  // streaming decode: heads prefetched into L2 ahead
-constexpr int kDefaultGroups = 2;      // streaming decode: consumer groups per CTA
+constexpr int kDefaultGroups = 2;      // streaming decode: consumer groups per CTA (FP32 state)
+constexpr int kDefaultGroupsBf16 = 4;  // BF16 state: four groups of four warps, state packed
 
 // Arguments of one fused decode step (layouts as documented in kda.h).
 struct DecodeArgs {
@@ -91,7 +92,9 @@ cudaError_t launch_decode(const DecodeArgs &a, int x_dtype, int state_dtype,
                           int columns, int threads, cudaStream_t stream);
 
 // Persistent streaming decode kernel (one CTA per SM, bulk-copy stages,
-// `groups` = 1 or 2 consumer groups). cudaErrorNotSupported for other groups.
+// `groups` = 1 or 2 consumer groups of 16 / 8 warps, or for BF16 state 4
+// groups of 4 warps with the state packed in registers).
+// cudaErrorNotSupported for other groups.
 cudaError_t launch_decode_stream(const DecodeArgs &a, int x_dtype, int state_dtype, int groups,
                                  cudaStream_t stream);
 

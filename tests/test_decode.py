@@ -135,6 +135,28 @@ def test_stream_kernel_ring_configs(K, groups, prefetch, state_dtype):
     _compare(dl, outs, ref, S, cache, _tol(state_dtype))
 
 
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("M,H", [(32, 64), (1, 1), (3, 7), (5, 64), (7, 61)])
+def test_packed_bf16_kernel(K, M, H, x_dtype):
+    """Four consumer groups of four warps with the BF16 state packed in
+    registers (stream kernel, groups = 4): full size, a single head, odd head
+    counts and ragged rounds, both input dtypes, two steps."""
+    inp = inputs.decode_layer(inputs.layer_seed(inputs.SEED_DECODE_STACK, 400 + M + H), M=M, H=H, T=2)
+    dl = DeviceLayer(inp, "bf16", x_dtype)
+    outs = _run(K, dl, 2, kernel=K.KDA_DECODE_STREAM, stream_cfg=(0, 4))
+    ref, S, cache = oracle_layer(inp)
+    _compare(dl, outs, ref, S, cache, TOL_BF16_STATE)
+
+
+def test_packed_kernel_needs_bf16_state(K):
+    """groups = 4 exists for BF16 state only: FP32 state is refused."""
+    inp = inputs.decode_layer(410, M=2, H=4, T=1)
+    dl = DeviceLayer(inp, "f32")
+    with pytest.raises(K.KdaError) as err:
+        _run(K, dl, 1, kernel=K.KDA_DECODE_STREAM, stream_cfg=(0, 4))
+    assert err.value.status == K.KDA_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("M,H", [(1, 1), (1, 5), (3, 7), (1, 64), (5, 64), (7, 61)])
 def test_stream_kernel_small_and_ragged(K, M, H):
     """Streaming kernel with fewer heads than SMs, odd head counts and a
