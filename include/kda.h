@@ -210,7 +210,10 @@ typedef enum {
                               columns) walks the sequence chunk by chunk */
     KDA_PREFILL_TC = 2     /* tensor-core chunk kernel (tcgen05, TF32 operands, FP32
                               accumulation): one CTA per (stream, head), state kept in
-                              tensor memory for the whole sequence */
+                              tensor memory across its chunks; with more (stream, head)
+                              pairs than SMs each sequence is cut into pieces of
+                              consecutive chunks run in rounds of kernel launches, the
+                              state passed between pieces in place (bit-identical) */
 } kda_prefill_kernel;
 
 /*
@@ -235,6 +238,9 @@ typedef enum {
  * inside FP32.
  * o must not overlap any input or the state; the state must not overlap any
  * input.
+ * The tensor-core path may issue several launches on `stream` (rounds of
+ * pieces, see kda_prefill_kernel); they are stream-ordered and capturable in
+ * a CUDA graph like a single launch.
  * The tensor-core kernel moves q, k, alpha, v and o by tiled tensor copies
  * through maps encoded on the host at each call (cuTensorMapEncodeTiled via
  * the runtime's driver entry point): a map the driver rejects (a stride of
@@ -248,8 +254,9 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, int qk
                              void *stream);
 
 /*
- * kda_prefill_layer — a KDA layer over a prompt of T tokens for M streams, one
- * launch on the tensor cores: the short conv + SiLU of the pre-conv q, k, v
+ * kda_prefill_layer — a KDA layer over a prompt of T tokens for M streams on
+ * the tensor cores (one launch, or rounds of pieces as kda_chunk_prefill):
+ * the short conv + SiLU of the pre-conv q, k, v
  * with the conv cache as left context, the forget gate from its raw input
  * (in log space), L2 norm of q and k, the chunked recurrence ("GLM-5.3 deep
  * dive" sections 8.2.3 - 8.2.5) and, optionally, the gated RMSNorm on every
