@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
@@ -492,6 +493,14 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 //   o_t = scale rq_t (Y_raw_t + sum_{j<=t} P_raw_tj d'_j),
 //   S_end = Gamma_last S0 + sum_j (k_raw_j R(last, j)) d'_j^T.
 // ---------------------------------------------------------------------------
+// Tensor maps of the staged inputs (encoded on the host per call): x as
+// [M][T][3][H*128] in boxes of 128 channels x 3 tensors x (CT + 3) tokens, and
+// alpha as [M][T][H][128] in boxes of 128 channels x CT tokens.
+struct TokMaps {
+    CUtensorMap x;
+    CUtensorMap alpha;
+};
+
 template <typename TS, typename TX>
 struct WyCfg {
     static constexpr int G = 2;
@@ -516,7 +525,8 @@ struct WyCfg {
     // [2][CT][128] and beta [2][CT] (by chunk parity: P3 of one chunk may still
     // read them while P1 of the next writes), Gamma q, Gamma k, k R(last, .)
     // [CT][VP], Gamma_last [VP], per token the P row, A row, rq, rk [CT][32],
-    // and with staged inputs x of tokens t0 - 3 .. t0 + CT - 1 [3][CT + 3][128]
+    // and with staged inputs x of tokens t0 - 3 .. t0 + CT - 1 [CT + 3][3][128]
+    // (the tensor copy's box order; XS and alpha start at 128-byte offsets)
     static constexpr int QK_F = 0;
     static constexpr int DXS = 2 * DK;             // row stride of the d' slots
     static constexpr int AL_F = QK_F + CT * 2 * DK;
@@ -538,8 +548,9 @@ struct WyCfg {
     static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
     static constexpr int SMEM = NST * STAGE + G * WORK_BYTES + BAR_BYTES;
     static_assert(NST >= 2, "at least two stages must fit");
-    static_assert(QD_F % 4 == 0 && XS_F % 4 == 0 && STAGE % 16 == 0 && WORK_BYTES % 16 == 0,
-                  "16-byte alignment");
+    static_assert(QD_F % 4 == 0 && STAGE % 16 == 0 && WORK_BYTES % 128 == 0 && XS_F % 32 == 0 &&
+                      AL_F % 32 == 0 && (NST * STAGE) % 128 == 0,
+                  "16-byte alignment; 128-byte tensor-copy destinations");
     static_assert(STAGE == TokCfg<TS, TX, G>::STAGE, "the stage layout of load_head_tokens");
 };
 
@@ -586,7 +597,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <typename TS, typename TX, bool MULTI>
 __global__ void __launch_bounds__(WyCfg<TS, TX>::THREADS, 1)
-kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
+kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_constant__ TokMaps mp) {
     using C = WyCfg<TS, TX>;
     constexpr int G = C::G, CT = C::CT, VP = C::VP;
     constexpr bool kRowPairs = sizeof(TS) == 2;
@@ -656,38 +667,21 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
     int par = 0;
     bool ok = true;
 
-    // Staged inputs of unit (uu, cn) (head uu, chunk cn): x of tokens
-    // t0 - 3 .. t0 + nc - 1 (from t0 for the first chunk, whose window starts in
-    // the conv cache) into [X][slot = token - t0 + 3], alpha of the chunk's
-    // tokens into the alpha buffer; completes on this group's input barrier.
+    // Staged inputs of unit (uu, cn) (head uu, chunk cn): two tensor copies
+    // issued by one thread, x of tokens t0 - 3 .. t0 + CT - 1 into [slot =
+    // token - t0 + 3][X][128] and alpha of tokens t0 .. t0 + CT - 1; tokens
+    // outside 0 .. T - 1 arrive as zeros (before token 0 the window comes from
+    // the conv cache instead). Completes on this group's input barrier.
     const TX *xsm = reinterpret_cast<const TX *>(buf + C::XS_F);
     uint32_t xk = 0;  // inputs consumed by this group
-    // Issued by the 32 lanes of the group's first warp, one or two copies each.
     auto stage_inputs = [&](int uu, int cn) {
         const int mm = uu / H, hh = uu - mm * H;
-        const int tt0 = cn * CT, ncn = min(CT, T - tt0);
-        const int first = cn == 0 ? tt0 : tt0 - 3, ntok = tt0 + ncn - first;
-        if (lane == 0)
-            ptx::mbar_arrive_expect_tx(&xin[g], 3u * (uint32_t)ntok * DK * sizeof(TX) +
-                                                    (uint32_t)ncn * DK * 4u);
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            int j = lane + 32 * r;
-            if (j < 3 * ntok) {
-                const int X2 = j / ntok, tau = first + j - X2 * ntok;
-                ptx::bulk_g2s(reinterpret_cast<unsigned char *>(buf + C::XS_F) +
-                                  (size_t)(X2 * (CT + 3) + tau - tt0 + 3) * DK * sizeof(TX),
-                              x + ((size_t)(mm * T + tau) * 3 + X2) * D + (size_t)hh * DK,
-                              DK * sizeof(TX), &xin[g]);
-            } else if ((j -= 3 * ntok) < ncn) {
-                ptx::bulk_g2s(buf + C::AL_F + j * DK,
-                              a.alpha + ((size_t)(mm * T + tt0 + j) * H + hh) * DK, DK * 4, &xin[g]);
-            }
-        }
-        if (lane == 0) xfills[g] = xfills[g] + 1u;
+        ptx::mbar_arrive_expect_tx(&xin[g], (uint32_t)C::XS_BYTES + CT * DK * 4u);
+        ptx::tma_load_4d(buf + C::XS_F, &mp.x, &xin[g], hh * DK, 0, cn * CT - 3, mm);
+        ptx::tma_load_4d(buf + C::AL_F, &mp.alpha, &xin[g], 0, hh, cn * CT, mm);
+        xfills[g] = xfills[g] + 1u;
     };
-    if (C::kStageX && cw == 0 && blockIdx.x + g * gridDim.x < n_units)
+    if (C::kStageX && ct == 0 && blockIdx.x + g * gridDim.x < n_units)
         stage_inputs(blockIdx.x + g * gridDim.x, 0);
 
     for (int i = g, u = blockIdx.x + g * gridDim.x; u < n_units; i += G, u += G * gridDim.x) {
@@ -732,14 +726,14 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
                 if (!landed) raise_error(8u);
 #pragma unroll
                 for (int j = 0; j < CT + 3; ++j)
-                    xq[j] = j < nc + 3 ? xsm[(X * (CT + 3) + j) * DK + ch] : zero_tx<TX>();
+                    xq[j] = j < nc + 3 ? xsm[(j * 3 + X) * DK + ch] : zero_tx<TX>();
 #pragma unroll
                 for (int j = 0; j < CT / 2 + 3; ++j)
-                    xv[j] = j < vn + 3 ? xsm[(2 * (CT + 3) + vb + j) * DK + ch] : zero_tx<TX>();
+                    xv[j] = j < vn + 3 ? xsm[((vb + j) * 3 + 2) * DK + ch] : zero_tx<TX>();
 #pragma unroll
                 for (int e = 0; e < 3; ++e) {
-                    cq[e] = last ? xsm[(X * (CT + 3) + nc + e) * DK + ch] : zero_tx<TX>();
-                    cv[e] = last ? xsm[(2 * (CT + 3) + nc + e) * DK + ch] : zero_tx<TX>();
+                    cq[e] = last ? xsm[((nc + e) * 3 + X) * DK + ch] : zero_tx<TX>();
+                    cv[e] = last ? xsm[((nc + e) * 3 + 2) * DK + ch] : zero_tx<TX>();
                 }
             } else {
 #pragma unroll
@@ -884,7 +878,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
                 }
             }
             ptx::named_bar_sync(bar_id, C::GT);  // the chunk's vectors and rows are ready
-            if (C::kStageX && cw == 0) {  // the staged inputs are read: stage the next chunk's
+            if (C::kStageX && ct == 0) {  // the staged inputs are read: stage the next chunk's
                 const bool more = c + 1 < nchunks;
                 const int un = more ? u : u + G * gridDim.x;
                 if (un < n_units) stage_inputs(un, more ? c + 1 : 0);
@@ -1098,9 +1092,9 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T) {
     }
 }
 
-template <typename KERNEL>
+template <typename KERNEL, typename... EXTRA>
 cudaError_t launch_persistent(KERNEL kernel, int threads, int smem, const DecodeArgs &a, int T,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const EXTRA &...extra) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1120,18 +1114,30 @@ cudaError_t launch_persistent(KERNEL kernel, int threads, int smem, const Decode
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a, T);
+    return cudaLaunchKernelEx(&cfg, kernel, a, T, extra...);
 }
 
 template <typename TS, typename TX>
 cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream) {
     if (T >= KDA_TOKENS_WY_MIN) {
         using C = WyCfg<TS, TX>;
+        TokMaps mp;
+        memset(&mp, 0, sizeof(mp));
+        if (C::kStageX) {
+            const uint64_t D = (uint64_t)a.H * DK;
+            const uint64_t dx[4] = {D, 3, (uint64_t)T, (uint64_t)a.M};
+            const uint32_t bx[4] = {DK, 3, C::CT + 3, 1};
+            const uint64_t da[4] = {DK, (uint64_t)a.H, (uint64_t)T, (uint64_t)a.M};
+            const uint32_t ba[4] = {DK, 1, C::CT, 1};
+            cudaError_t e = make_tensor_map(&mp.x, a.x, sizeof(TX) == 2, 4, dx, bx, false);
+            if (e == cudaSuccess) e = make_tensor_map(&mp.alpha, a.alpha, false, 4, da, ba, false);
+            if (e != cudaSuccess) return e;
+        }
         if (T > C::CT)
             return launch_persistent(kda_decode_tokens_wy_kernel<TS, TX, true>, C::THREADS, C::SMEM, a, T,
-                                     stream);
+                                     stream, mp);
         return launch_persistent(kda_decode_tokens_wy_kernel<TS, TX, false>, C::THREADS, C::SMEM, a, T,
-                                 stream);
+                                 stream, mp);
     }
     using C = TokCfg<TS, TX, 2>;
     return launch_persistent(kda_decode_tokens_kernel<TS, TX, 2>, C::THREADS, C::SMEM, a, T, stream);
