@@ -475,9 +475,9 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 // Per chunk a group runs three phases:
 //  P1 (thread per channel): conv + SiLU of the chunk's q, k (one channel
 //     each) and v (one channel, half the tokens), alpha and beta into shared
-//     memory (with FP32 state and BF16 inputs, x and alpha of the chunk were
-//     copied into shared memory by bulk copies the group's first warp issued
-//     one chunk earlier, on a per-group mbarrier);              group barrier
+//     memory (with BF16 inputs, x and alpha of the chunk were copied into
+//     shared memory by two tensor copies one thread issued one chunk earlier,
+//     on a per-group mbarrier);                                 group barrier
 //  P2 (warp t per token t): the norms of q_t, k_t, the rows A_t. and P_t. (raw,
 //     unnormalised), and Gamma_t q_t, Gamma_t k_t, k_t R(last, t), Gamma_last
 //     into row-permuted buffers;                                group barrier
@@ -512,10 +512,9 @@ struct WyCfg {
     static constexpr int S_BYTES = DK * DK * (int)sizeof(TS);
     static constexpr int C_OFF = S_BYTES;
     static constexpr int STAGE = C_OFF + 9 * DK * (int)sizeof(TX);
-    // With FP32 state and BF16 inputs, the next chunk's inputs are staged in
-    // shared memory by bulk copies issued a chunk ahead (FP32 inputs would need
-    // twice the room; with BF16 state the direct loads measured faster)
-    static constexpr bool kStageX = sizeof(TX) == 2 && sizeof(TS) == 4;
+    // With BF16 inputs the next chunk's inputs are staged in shared memory by
+    // tensor copies issued a chunk ahead (FP32 inputs would need twice the room)
+    static constexpr bool kStageX = sizeof(TX) == 2;
     // row-permuted vectors: lane group rl's 16 rows at 16 rl + 4 (rl / 2), so
     // the 8 groups' 16-byte reads fall into 8 different bank quads
     static constexpr int VP = 144;
