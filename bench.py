@@ -611,7 +611,7 @@ def time_tokens(torch, kda, inputs, M, T, state_dtype, K, W):
 
 # Calls of at least this many tokens run the chunked multi-token kernel (the
 # library's dispatch rule in kda_decode_tokens.cu).
-TOKENS_WY_MIN = 4
+TOKENS_WY_MIN = 3
 
 
 def tokens_kernel_name(T):

@@ -161,7 +161,7 @@ kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w
  *                               when stored at the end of the call.
  *   o           [M, T, H, dv]   FP32 outputs of every token
  *   T >= 1 (state traffic is amortised over T; the arithmetic grows with T,
- *   so for long inputs the chunked prefill is the faster path). Calls of 4
+ *   so for long inputs the chunked prefill is the faster path). Calls of 3
  *   or more tokens regroup the recurrence into chunks of up to 8 tokens
  *   (section 8.2.4's WY form, FP32 throughout): results agree with the
  *   token-by-token order to FP32 rounding, and two calls split at a multiple

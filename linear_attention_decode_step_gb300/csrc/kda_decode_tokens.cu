@@ -29,7 +29,7 @@
 // Calls of at least this many tokens take the chunked kernel, shorter ones
 // the token-by-token kernel.
 #ifndef KDA_TOKENS_WY_MIN
-#define KDA_TOKENS_WY_MIN 4
+#define KDA_TOKENS_WY_MIN 3
 #endif
 
 namespace kda {
