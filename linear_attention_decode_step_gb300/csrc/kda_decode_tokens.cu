@@ -477,10 +477,12 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 //     each) and v (one channel, half the tokens), alpha and beta into shared
 //     memory (with BF16 inputs, x and alpha of the chunk were copied into
 //     shared memory by two tensor copies one thread issued one chunk earlier,
-//     on a per-group mbarrier);                                 group barrier
+//     on a per-group mbarrier; with FP32 state the head's conv cache comes
+//     with its first chunk's inputs in a third one);            group barrier
 //  P2 (warp t per token t): the norms of q_t, k_t, the rows A_t. and P_t. (raw,
 //     unnormalised), and Gamma_t q_t, Gamma_t k_t, k_t R(last, t), Gamma_last
-//     into row-permuted buffers;                                group barrier
+//     into row-permuted buffers; at a head's first chunk the state from its
+//     stage into registers;                                     group barrier
 //  P3 (the state in registers, warp cw owning value columns 16 cw .. + 15 of
 //     all 128 key rows as in the token-by-token kernel): one pass forms the
 //     2 x CT column sums (Gamma k) . S0 and (Gamma q) . S0 and reduces them
@@ -494,11 +496,13 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 //   S_end = Gamma_last S0 + sum_j (k_raw_j R(last, j)) d'_j^T.
 // ---------------------------------------------------------------------------
 // Tensor maps of the staged inputs (encoded on the host per call): x as
-// [M][T][3][H*128] in boxes of 128 channels x 3 tensors x (CT + 3) tokens, and
-// alpha as [M][T][H][128] in boxes of 128 channels x CT tokens.
+// [M][T][3][H*128] in boxes of 128 channels x 3 tensors x (CT + 3) tokens,
+// alpha as [M][T][H][128] in boxes of 128 channels x CT tokens, and (FP32
+// state) the conv cache as [M][9][H*128] in boxes of 128 channels x 9 taps.
 struct TokMaps {
     CUtensorMap x;
     CUtensorMap alpha;
+    CUtensorMap cache;
 };
 
 template <typename TS, typename TX>
@@ -509,12 +513,16 @@ struct WyCfg {
     static constexpr int THREADS = kWarps * 32;
     static constexpr int CT = 8;                       // tokens per chunk: one per warp in P2
     static_assert(CT == CWARPS && CWARPS * 16 == DK, "one warp per token, 16 columns per warp");
+    // With BF16 inputs the next chunk's inputs are staged in shared memory by
+    // tensor copies issued a chunk ahead (FP32 inputs would need twice the room);
+    static constexpr bool kStageX = sizeof(TX) == 2;
+    // With FP32 state (one stage per group) the conv cache arrives with them
+    // too, so a stage holds only the state and is waited for where it is read
+    // (BF16 state: two stages per group arrive early enough; measured slower)
+    static constexpr bool kCacheX = kStageX && sizeof(TS) == 4;
     static constexpr int S_BYTES = DK * DK * (int)sizeof(TS);
     static constexpr int C_OFF = S_BYTES;
-    static constexpr int STAGE = C_OFF + 9 * DK * (int)sizeof(TX);
-    // With BF16 inputs the next chunk's inputs are staged in shared memory by
-    // tensor copies issued a chunk ahead (FP32 inputs would need twice the room)
-    static constexpr bool kStageX = sizeof(TX) == 2;
+    static constexpr int STAGE = kCacheX ? S_BYTES : C_OFF + 9 * DK * (int)sizeof(TX);
     // row-permuted vectors: lane group rl's 16 rows at 16 rl + 4 (rl / 2), so
     // the 8 groups' 16-byte reads fall into 8 different bank quads
     static constexpr int VP = 144;
@@ -538,7 +546,9 @@ struct WyCfg {
     static constexpr int RED_F = GL_F + VP;
     static constexpr int XS_F = RED_F + CT * 32;
     static constexpr int XS_BYTES = kStageX ? 3 * (CT + 3) * DK * (int)sizeof(TX) : 0;
-    static constexpr int WORK_F = XS_F + XS_BYTES / 4;
+    static constexpr int CS_F = XS_F + XS_BYTES / 4;
+    static constexpr int CS_BYTES = kCacheX ? 9 * DK * (int)sizeof(TX) : 0;
+    static constexpr int WORK_F = CS_F + CS_BYTES / 4;
     static constexpr int WORK_BYTES = WORK_F * 4;
     // full[8], issued[8], fills[8], then the input barriers xin[2] and their
     // fill counts [2]
@@ -550,8 +560,22 @@ struct WyCfg {
     static_assert(QD_F % 4 == 0 && STAGE % 16 == 0 && WORK_BYTES % 128 == 0 && XS_F % 32 == 0 &&
                       AL_F % 32 == 0 && (NST * STAGE) % 128 == 0,
                   "16-byte alignment; 128-byte tensor-copy destinations");
-    static_assert(STAGE == TokCfg<TS, TX, G>::STAGE, "the stage layout of load_head_tokens");
+    static_assert(kCacheX || STAGE == TokCfg<TS, TX, G>::STAGE, "the stage layout of load_head_tokens");
+    static_assert(CS_F % 32 == 0, "128-byte tensor-copy destination");
 };
+
+// A stage of the chunked kernel: the head's state (and, unless the conv cache
+// arrives with the staged inputs, the cache as in load_head_tokens).
+template <typename TS, typename TX, typename C>
+__device__ __forceinline__ void load_stage_wy(unsigned char *st, uint64_t *bar, const DecodeArgs &a, int u,
+                                              uint64_t pol) {
+    if constexpr (C::kCacheX) {
+        ptx::mbar_arrive_expect_tx(bar, C::S_BYTES);
+        ptx::bulk_g2s_hint(st, static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES, bar, pol);
+    } else {
+        load_head_tokens<TS, TX, C::G>(st, bar, a, u, pol);
+    }
+}
 
 __device__ __forceinline__ int wy_base(int rl) { return 16 * rl + 4 * (rl >> 1); }
 __device__ __forceinline__ int wy_pos(int i) { return wy_base(i & 7) + (i >> 3); }
@@ -638,7 +662,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
             const int u = blockIdx.x + s * gridDim.x;
-            if (u < n_units) load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, u, pol);
+            if (u < n_units) load_stage_wy<TS, TX, C>(smem + s * C::STAGE, &full[s], a, u, pol);
         }
     }
 
@@ -675,9 +699,11 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
     uint32_t xk = 0;  // inputs consumed by this group
     auto stage_inputs = [&](int uu, int cn) {
         const int mm = uu / H, hh = uu - mm * H;
-        ptx::mbar_arrive_expect_tx(&xin[g], (uint32_t)C::XS_BYTES + CT * DK * 4u);
+        ptx::mbar_arrive_expect_tx(&xin[g], (uint32_t)C::XS_BYTES + CT * DK * 4u +
+                                                (cn == 0 ? (uint32_t)C::CS_BYTES : 0u));
         ptx::tma_load_4d(buf + C::XS_F, &mp.x, &xin[g], hh * DK, 0, cn * CT - 3, mm);
         ptx::tma_load_4d(buf + C::AL_F, &mp.alpha, &xin[g], 0, hh, cn * CT, mm);
+        if (C::kCacheX && cn == 0) ptx::tma_load_4d(buf + C::CS_F, &mp.cache, &xin[g], hh * DK, 0, mm, 0);
         xfills[g] = xfills[g] + 1u;
     };
     if (C::kStageX && ct == 0 && blockIdx.x + g * gridDim.x < n_units)
@@ -688,7 +714,8 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
         const int m = u / H, h = u - m * H;
         const size_t hb = (size_t)h * DK;
         const TS *Ss = reinterpret_cast<const TS *>(smem + s * C::STAGE);
-        const TX *cs = reinterpret_cast<const TX *>(smem + s * C::STAGE + C::C_OFF);
+        const TX *cs = C::kCacheX ? reinterpret_cast<const TX *>(buf + C::CS_F)
+                                  : reinterpret_cast<const TX *>(smem + s * C::STAGE + C::C_OFF);
         const TX *xqk = x + ((size_t)m * T * 3 + X) * D + hb + ch;
         const TX *xvv = x + ((size_t)m * T * 3 + 2) * D + hb + ch;
         // The lane's 64 state values as FP32 pairs. BF16 storage: sv[4 p + e] =
@@ -718,7 +745,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
                 // this chunk's inputs landed (issued a chunk ahead)
                 landed = ptx::mbar_wait(&xin[g], xk & 1, ptx::kWaitBudget);
                 ++xk;
-                if (c == 0)  // the stage's refill was issued, then its bytes landed
+                if (!C::kCacheX && c == 0)  // the stage's refill was issued, then its bytes landed
                     landed = landed &&
                              (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
                              ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
@@ -799,7 +826,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
             } else {
                 ptx::named_bar_sync(bar_id, C::GT);
             }
-            if (last) {
+            if (!C::kCacheX && last) {
                 const size_t cbase = (size_t)m * 9 * D + hb;
 #pragma unroll
                 for (int e = 0; e < 3; ++e) {
@@ -856,6 +883,14 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
                     rr[17] = rsqrtf(kk + kL2Eps);
                 }
             }
+            // with the cache staged with the inputs the state is waited for only
+            // here, where it is read
+            bool slanded = true;
+            if (C::kCacheX && c == 0) {
+                slanded = (n == 0 || ptx::mbar_wait(&issued[s], (n - 1) & 1, ptx::kWaitBudget)) &&
+                          ptx::mbar_wait(&full[s], n & 1, ptx::kWaitBudget);
+                if (!slanded) raise_error(8u);
+            }
             if (c == 0) {
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
@@ -876,7 +911,24 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
                     }
                 }
             }
-            ptx::named_bar_sync(bar_id, C::GT);  // the chunk's vectors and rows are ready
+            // the chunk's vectors and rows are ready (and every thread's wait for the
+            // state succeeded)
+            if (C::kCacheX && c == 0) {
+                if (!ptx::named_bar_and(bar_id, C::GT, slanded)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                ptx::named_bar_sync(bar_id, C::GT);
+            }
+            if (C::kCacheX && last) {  // after every wait of the chunk succeeded
+                const size_t cbase = (size_t)m * 9 * D + hb;
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    cache[cbase + (size_t)(3 * X + e) * D + ch] = cq[e];
+                    if (vh) cache[cbase + (size_t)(6 + e) * D + ch] = cv[e];
+                }
+            }
             if (C::kStageX && ct == 0) {  // the staged inputs are read: stage the next chunk's
                 const bool more = c + 1 < nchunks;
                 const int un = more ? u : u + G * gridDim.x;
@@ -885,7 +937,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
             if (c == 0 && ct == 0) {             // the stage is read: refill it
                 const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
                 if (ur < n_units) {
-                    load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                    load_stage_wy<TS, TX, C>(smem + s * C::STAGE, &full[s], a, ur, pol);
                     fills[s] = fills[s] + 1u;
                     ptx::mbar_arrive(&issued[s]);
                 }
@@ -1130,6 +1182,9 @@ cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream)
             const uint32_t ba[4] = {DK, 1, C::CT, 1};
             cudaError_t e = make_tensor_map(&mp.x, a.x, sizeof(TX) == 2, 4, dx, bx, false);
             if (e == cudaSuccess) e = make_tensor_map(&mp.alpha, a.alpha, false, 4, da, ba, false);
+            const uint64_t dc[4] = {D, 9, (uint64_t)a.M, 1};
+            const uint32_t bc[4] = {DK, 9, 1, 1};
+            if (e == cudaSuccess && C::kCacheX) e = make_tensor_map(&mp.cache, a.cache, true, 4, dc, bc, false);
             if (e != cudaSuccess) return e;
         }
         if (T > C::CT)
