@@ -8,8 +8,10 @@
 //  * One CTA per SM loops over whole heads (stream m, head h); a head's state
 //    is one contiguous block (64 KiB FP32, 32 KiB BF16).
 //  * Each head's state, alpha, pre-conv x and conv-cache taps are copied into
-//    a ring of NST shared-memory stages with cp.async.bulk; the copies
-//    complete on the stage's "full" mbarrier (transaction bytes).
+//    a ring of NST shared-memory stages (state and alpha by cp.async.bulk, x
+//    and the cache by one tensor copy each, or with FP32 state beyond 1024
+//    heads by a bulk copy per row); the copies complete on the stage's
+//    "full" mbarrier (transaction bytes).
 //  * The CTA's 16 warps form G consumer groups (G = 1 or 2) that take heads
 //    in turn (group g: heads g, g + G, ...). A group pulls its stage into
 //    registers and convolves the head's 3 x 128 channels from the same stage;
@@ -66,6 +68,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
@@ -173,21 +176,38 @@ __device__ __forceinline__ void prefetch_head(const DecodeArgs &a, int u) {
                           DK * DK * sizeof(TS));
 }
 
-// Issues the bulk copies of head u into stage `st`, completing on `bar`
-// (without alpha when the fused gate computes it).
+// Tensor maps of one call's pre-conv inputs and conv cache (encoded on the
+// host per call when `on`): x as [M][3][H*128] and the cache as [M][9][H*128],
+// in boxes of 128 channels x 3 or 9 rows, so a head's q, k, v inputs and its
+// nine cached taps arrive in one tensor copy each instead of twelve bulk
+// copies issued one after another.
+struct DecMaps {
+    CUtensorMap x;
+    CUtensorMap cache;
+    int on;
+};
+
+// Issues the copies of head u into stage `st`, completing on `bar`: the state
+// and alpha (not with the fused gate, which computes it) by bulk copies, x and
+// the conv cache by tensor copies or, without maps, by a bulk copy per row.
 template <typename TS, typename TX, int G, bool GATE>
 __device__ __forceinline__ void load_head(unsigned char *st, uint64_t *bar, const DecodeArgs &a,
-                                          int u, uint64_t pol) {
+                                          const DecMaps &mp, int u, uint64_t pol) {
     using C = Cfg<TS, TX, G>;
     const int H = a.H;
     const size_t D = (size_t)H * DK;
     const int m = u / H, h = u - m * H;
-    const TX *x = static_cast<const TX *>(a.x);
-    const TX *cache = static_cast<const TX *>(a.cache);
     ptx::mbar_arrive_expect_tx(bar, GATE ? C::STAGE - DK * 4 : C::STAGE);
     ptx::bulk_g2s_hint(st, static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES, bar,
                        pol);
     if (!GATE) ptx::bulk_g2s(st + C::A_OFF, a.alpha + (size_t)u * DK, DK * 4, bar);
+    if (mp.on) {
+        ptx::tma_load_4d(st + C::X_OFF, &mp.x, bar, h * DK, 0, m, 0);
+        ptx::tma_load_4d(st + C::C_OFF, &mp.cache, bar, h * DK, 0, m, 0);
+        return;
+    }
+    const TX *x = static_cast<const TX *>(a.x);
+    const TX *cache = static_cast<const TX *>(a.cache);
 #pragma unroll
     for (int X = 0; X < 3; ++X)
         ptx::bulk_g2s(st + C::X_OFF + X * DK * sizeof(TX), x + ((size_t)m * 3 + X) * D + (size_t)h * DK,
@@ -198,9 +218,29 @@ __device__ __forceinline__ void load_head(unsigned char *st, uint64_t *bar, cons
                       DK * sizeof(TX), bar);
 }
 
+// Up to this many heads, FP32-state calls take x and the cache by tensor
+// copies (measured on the 34-layer stack: 5 % faster at M = 1, 2 % at M = 8,
+// 1.6 % slower at M = 32, where the layer is bound by HBM); BF16-state calls
+// always do (1-4 % faster at every M).
+constexpr int kTensorInputsMaxHeadsF32 = 1024;
+
+// The tensor maps of a decode call, encoded only if the call uses them.
+template <typename TX>
+cudaError_t make_decode_maps(DecMaps *mp, const DecodeArgs &a, bool on) {
+    memset(mp, 0, sizeof(*mp));
+    if (!on) return cudaSuccess;
+    const uint64_t D = (uint64_t)a.H * DK;
+    const uint64_t dx[4] = {D, 3, (uint64_t)a.M, 1}, dc[4] = {D, 9, (uint64_t)a.M, 1};
+    const uint32_t bx[4] = {DK, 3, 1, 1}, bc[4] = {DK, 9, 1, 1};
+    cudaError_t e = make_tensor_map(&mp->x, a.x, sizeof(TX) == 2, 4, dx, bx, false);
+    if (e == cudaSuccess) e = make_tensor_map(&mp->cache, a.cache, sizeof(TX) == 2, 4, dc, bc, false);
+    mp->on = 1;
+    return e;
+}
+
 template <typename TS, typename TX, int G, bool GATE, bool NORM>
 __global__ void __launch_bounds__(Cfg<TS, TX, G>::THREADS, 1)
-kda_decode_stream_kernel(const DecodeArgs a) {
+kda_decode_stream_kernel(const DecodeArgs a, const __grid_constant__ DecMaps mp) {
     using C = Cfg<TS, TX, G>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
@@ -240,7 +280,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
             const int u = blockIdx.x + s * gridDim.x;
-            if (u < n_units) load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, u, pol);
+            if (u < n_units) load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, mp, u, pol);
         }
         for (int j = 0; j < P; ++j) {
             const int u = blockIdx.x + (C::NST + j) * gridDim.x;
@@ -358,7 +398,7 @@ kda_decode_stream_kernel(const DecodeArgs a) {
         if (ct == 0) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;  // refill with head i + NST
             if (ur < n_units) {
-                load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                load_head<TS, TX, G, GATE>(smem + s * C::STAGE, &full[s], a, mp, ur, pol);
                 fills[s] = fills[s] + 1u;
                 ptx::mbar_arrive(&issued[s]);
                 const int up = ur + P * gridDim.x;
@@ -583,7 +623,7 @@ struct PCfg {
 
 template <typename TX>
 __global__ void __launch_bounds__(PCfg<TX>::THREADS, 1)
-kda_decode_packed_kernel(const DecodeArgs a) {
+kda_decode_packed_kernel(const DecodeArgs a, const __grid_constant__ DecMaps mp) {
     using C = PCfg<TX>;
     using TS = __nv_bfloat16;
     constexpr int G = C::G;
@@ -616,7 +656,7 @@ kda_decode_packed_kernel(const DecodeArgs a) {
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
             const int u = blockIdx.x + s * gridDim.x;
-            if (u < n_units) load_head<TS, TX, 2, false>(smem + s * C::STAGE, &full[s], a, u, pol);
+            if (u < n_units) load_head<TS, TX, 2, false>(smem + s * C::STAGE, &full[s], a, mp, u, pol);
         }
     }
 
@@ -692,7 +732,7 @@ kda_decode_packed_kernel(const DecodeArgs a) {
         if (ct == 0) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;  // refill with head i + NST
             if (ur < n_units) {
-                load_head<TS, TX, 2, false>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                load_head<TS, TX, 2, false>(smem + s * C::STAGE, &full[s], a, mp, ur, pol);
                 fills[s] = fills[s] + 1u;
                 ptx::mbar_arrive(&issued[s]);
             }
@@ -810,6 +850,9 @@ cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    DecMaps mp;
+    e = make_decode_maps<TX>(&mp, a, sizeof(TS) == 2 || a.M * a.H <= kTensorInputsMaxHeadsF32);
+    if (e != cudaSuccess) return e;
     const int units = a.M * a.H;
     const int grid = units < sms ? units : sms;
     cudaLaunchConfig_t cfg = {};
@@ -822,7 +865,7 @@ cudaError_t launch_stream_typed(const DecodeArgs &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
+    return cudaLaunchKernelEx(&cfg, kernel, a, mp);
 }
 
 template <typename TX>
@@ -836,6 +879,9 @@ cudaError_t launch_packed_typed(const DecodeArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    DecMaps mp;
+    e = make_decode_maps<TX>(&mp, a, true);
+    if (e != cudaSuccess) return e;
     const int units = a.M * a.H;
     const int grid = units < sms ? units : sms;
     cudaLaunchConfig_t cfg = {};
@@ -848,7 +894,7 @@ cudaError_t launch_packed_typed(const DecodeArgs &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
+    return cudaLaunchKernelEx(&cfg, kernel, a, mp);
 }
 
 template <typename TS, typename TX>
