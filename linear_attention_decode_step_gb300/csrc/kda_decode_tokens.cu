@@ -124,10 +124,19 @@ template <> struct Quad<__nv_bfloat16> {
     }
 };
 
-// Bulk copies of head u's state and conv cache into stage `st`.
+// Copies of head u's state (one bulk copy) and conv cache into stage `st`:
+// the cache by one tensor copy through `cmap` ([M][9][H*128] in boxes of 128
+// channels x 9 taps) or, without a map, by nine bulk copies of a row each.
+// The conv cache's tensor map for the token-by-token kernel, used when `on`.
+struct TokCacheMap {
+    CUtensorMap map;
+    int on;
+};
+
 template <typename TS, typename TX, int G>
 __device__ __forceinline__ void load_head_tokens(unsigned char *st, uint64_t *bar,
-                                                 const DecodeArgs &a, int u, uint64_t pol) {
+                                                 const DecodeArgs &a, int u, uint64_t pol,
+                                                 const CUtensorMap *cmap) {
     using C = TokCfg<TS, TX, G>;
     const int H = a.H;
     const size_t D = (size_t)H * DK;
@@ -136,6 +145,10 @@ __device__ __forceinline__ void load_head_tokens(unsigned char *st, uint64_t *ba
     ptx::mbar_arrive_expect_tx(bar, C::STAGE);
     ptx::bulk_g2s_hint(st, static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES, bar,
                        pol);
+    if (cmap) {
+        ptx::tma_load_4d(st + C::C_OFF, cmap, bar, h * DK, 0, m, 0);
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < 9; ++j)
         ptx::bulk_g2s(st + C::C_OFF + j * DK * sizeof(TX),
@@ -169,7 +182,7 @@ __device__ __noinline__ void drain_fills(unsigned char *smem) {
 
 template <typename TS, typename TX, int G>
 __global__ void __launch_bounds__(TokCfg<TS, TX, G>::THREADS, 1)
-kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
+kda_decode_tokens_kernel(const DecodeArgs a, const int T, const __grid_constant__ TokCacheMap cm) {
     using C = TokCfg<TS, TX, G>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::NST * C::STAGE + G * C::WORK_BYTES);
@@ -207,7 +220,7 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
             const int u = blockIdx.x + s * gridDim.x;
-            if (u < n_units) load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, u, pol);
+            if (u < n_units) load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, u, pol, cm.on ? &cm.map : nullptr);
         }
     }
 
@@ -326,7 +339,7 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
         if (ct == 0 && go) {
             const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
             if (ur < n_units) {
-                load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                load_head_tokens<TS, TX, G>(smem + s * C::STAGE, &full[s], a, ur, pol, cm.on ? &cm.map : nullptr);
                 fills[s] = fills[s] + 1u;
                 ptx::mbar_arrive(&issued[s]);
             }
@@ -497,8 +510,9 @@ kda_decode_tokens_kernel(const DecodeArgs a, const int T) {
 // ---------------------------------------------------------------------------
 // Tensor maps of the staged inputs (encoded on the host per call): x as
 // [M][T][3][H*128] in boxes of 128 channels x 3 tensors x (CT + 3) tokens,
-// alpha as [M][T][H][128] in boxes of 128 channels x CT tokens, and (FP32
-// state) the conv cache as [M][9][H*128] in boxes of 128 channels x 9 taps.
+// alpha as [M][T][H][128] in boxes of 128 channels x CT tokens, and the conv
+// cache as [M][9][H*128] in boxes of 128 channels x 9 taps (FP32 state: with
+// a head's first chunk of inputs; BF16 state: into the head's stage).
 struct TokMaps {
     CUtensorMap x;
     CUtensorMap alpha;
@@ -567,13 +581,13 @@ struct WyCfg {
 // A stage of the chunked kernel: the head's state (and, unless the conv cache
 // arrives with the staged inputs, the cache as in load_head_tokens).
 template <typename TS, typename TX, typename C>
-__device__ __forceinline__ void load_stage_wy(unsigned char *st, uint64_t *bar, const DecodeArgs &a, int u,
-                                              uint64_t pol) {
+__device__ __forceinline__ void load_stage_wy(unsigned char *st, uint64_t *bar, const DecodeArgs &a,
+                                              const TokMaps &mp, int u, uint64_t pol) {
     if constexpr (C::kCacheX) {
         ptx::mbar_arrive_expect_tx(bar, C::S_BYTES);
         ptx::bulk_g2s_hint(st, static_cast<const TS *>(a.state) + (size_t)u * DK * DK, C::S_BYTES, bar, pol);
     } else {
-        load_head_tokens<TS, TX, C::G>(st, bar, a, u, pol);
+        load_head_tokens<TS, TX, C::G>(st, bar, a, u, pol, C::kStageX ? &mp.cache : nullptr);
     }
 }
 
@@ -662,7 +676,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
             const int u = blockIdx.x + s * gridDim.x;
-            if (u < n_units) load_stage_wy<TS, TX, C>(smem + s * C::STAGE, &full[s], a, u, pol);
+            if (u < n_units) load_stage_wy<TS, TX, C>(smem + s * C::STAGE, &full[s], a, mp, u, pol);
         }
     }
 
@@ -937,7 +951,7 @@ kda_decode_tokens_wy_kernel(const DecodeArgs a, const int T, const __grid_consta
             if (c == 0 && ct == 0) {             // the stage is read: refill it
                 const int ur = blockIdx.x + (i + C::NST) * gridDim.x;
                 if (ur < n_units) {
-                    load_stage_wy<TS, TX, C>(smem + s * C::STAGE, &full[s], a, ur, pol);
+                    load_stage_wy<TS, TX, C>(smem + s * C::STAGE, &full[s], a, mp, ur, pol);
                     fills[s] = fills[s] + 1u;
                     ptx::mbar_arrive(&issued[s]);
                 }
@@ -1184,7 +1198,7 @@ cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream)
             if (e == cudaSuccess) e = make_tensor_map(&mp.alpha, a.alpha, false, 4, da, ba, false);
             const uint64_t dc[4] = {D, 9, (uint64_t)a.M, 1};
             const uint32_t bc[4] = {DK, 9, 1, 1};
-            if (e == cudaSuccess && C::kCacheX) e = make_tensor_map(&mp.cache, a.cache, true, 4, dc, bc, false);
+            if (e == cudaSuccess) e = make_tensor_map(&mp.cache, a.cache, true, 4, dc, bc, false);
             if (e != cudaSuccess) return e;
         }
         if (T > C::CT)
@@ -1194,7 +1208,19 @@ cudaError_t launch_tokens_typed(const DecodeArgs &a, int T, cudaStream_t stream)
                                  stream, mp);
     }
     using C = TokCfg<TS, TX, 2>;
-    return launch_persistent(kda_decode_tokens_kernel<TS, TX, 2>, C::THREADS, C::SMEM, a, T, stream);
+    // the cache by one tensor copy per head: faster with BF16 state (M = 32,
+    // T = 2: 44.0 -> 43.1 us) and with FP32 state from 1024 heads on (49.6 ->
+    // 49.0), slower with FP32 state at M = 8 (15.2 -> 15.5)
+    TokCacheMap cm;
+    memset(&cm, 0, sizeof(cm));
+    if (sizeof(TS) == 2 || a.M * a.H >= 1024) {
+        const uint64_t dc[4] = {(uint64_t)a.H * DK, 9, (uint64_t)a.M, 1};
+        const uint32_t bc[4] = {DK, 9, 1, 1};
+        const cudaError_t e = make_tensor_map(&cm.map, a.cache, sizeof(TX) == 2, 4, dc, bc, false);
+        if (e != cudaSuccess) return e;
+        cm.on = 1;
+    }
+    return launch_persistent(kda_decode_tokens_kernel<TS, TX, 2>, C::THREADS, C::SMEM, a, T, stream, cm);
 }
 
 }  // namespace
