@@ -108,6 +108,12 @@ kda_status kda_conv_step(const void *x, int x_dtype, const float *conv_w,
  *   and M * H <= 2^30 (KDA_ERR_UNSUPPORTED beyond).
  * The buffers the call writes (o, state, conv_cache) must not overlap each
  * other or any input; an overlap returns KDA_ERR_INVALID_ARG.
+ * The streaming kernel reads x and the conv cache by tiled tensor copies
+ * through maps encoded on the host at each call (cuTensorMapEncodeTiled via
+ * the runtime's driver entry point), with BF16 state and, with FP32 state,
+ * up to 1024 heads; a driver without that entry point returns
+ * KDA_ERR_UNSUPPORTED before any launch. Under CUDA-graph capture the maps
+ * are part of the captured launch.
  */
 kda_status kda_decode_step(const void *x, int x_dtype, const float *conv_w,
                            void *conv_cache, int cache_dtype,
@@ -167,6 +173,10 @@ kda_status kda_decode_step_fused(const void *x, int x_dtype, const float *conv_w
  *   token-by-token order to FP32 rounding, and two calls split at a multiple
  *   of 8 tokens reproduce one call bit for bit.
  * Other arguments, checks and errors as kda_decode_step (sizes scale with T).
+ * The chunked kernel stages x, alpha and the conv cache by tiled tensor
+ * copies through maps encoded at each call (with BF16 x), and the
+ * token-by-token kernel the conv cache (BF16 state, or FP32 state from 1024
+ * heads); a map the driver rejects returns KDA_ERR_CUDA before any launch.
  */
 kda_status kda_decode_tokens(const void *x, int x_dtype, const float *conv_w,
                              void *conv_cache, int cache_dtype,
