@@ -75,10 +75,12 @@ def test_tokens_dtypes(K, state_dtype, x_dtype):
 
 
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-def test_tokens_M32_full_heads(K, state_dtype):
-    """M = 32 streams x 64 heads (the decode workload), 4 tokens: every output
-    and the whole final state against the oracle."""
-    _check(K, 32, 64, 4, state_dtype, seed=40)
+@pytest.mark.parametrize("T", [2, 4])
+def test_tokens_M32_full_heads(K, state_dtype, T):
+    """M = 32 streams x 64 heads (the decode workload), 2 tokens (token by
+    token, the conv cache by a tensor copy) and 4 (chunked): every output and
+    the whole final state against the oracle."""
+    _check(K, 32, 64, T, state_dtype, seed=40 + T)
 
 
 def test_tokens_single_stream_single_head(K):
