@@ -199,7 +199,8 @@ typedef enum {
  * columns are split into slices of `columns` (16, 32, 64 or 128), one CTA of
  * `threads` threads each. With KDA_DECODE_STREAM, `columns` is the number of
  * heads (0-16) whose state is prefetched into L2 ahead of the shared-memory
- * ring and `threads` the number of consumer groups per CTA (1 or 2, or 4
+ * ring (kda_decode_step uses 2 with FP32 state from 768 to 2048 heads, else
+ * 0) and `threads` the number of consumer groups per CTA (1 or 2, or 4
  * with BF16 state: four groups of four warps holding the state packed; 0
  * picks the default: 2 for FP32 state, 4 for BF16). With `threads` = 4 the
  * L2 prefetch count is ignored.

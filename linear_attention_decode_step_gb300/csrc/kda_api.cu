@@ -162,7 +162,11 @@ kda_status kda_decode_step_config(const void *x, int x_dtype, const float *conv_
     a.M = M;
     a.H = H;
     a.scale = scale;
-    a.l2_prefetch = kda::kDefaultL2Prefetch;
+    const long long heads = (long long)M * H;
+    a.l2_prefetch = state_dtype == KDA_F32 && heads >= kda::kL2PrefetchMinHeads &&
+                            heads <= kda::kL2PrefetchMaxHeads
+                        ? kda::kL2PrefetchMid
+                        : kda::kDefaultL2Prefetch;
     // BF16 state: four groups of four warps with the state packed in registers
     int groups = state_dtype == KDA_BF16 ? kda::kDefaultGroupsBf16 : kda::kDefaultGroups;
     if (explicit_kernel && kernel == KDA_DECODE_STREAM) {

@@ -11,6 +11,11 @@ namespace kda {
 
 constexpr int kHeadDim = 128;  // dk = dv handled by the decode and prefill kernels
 constexpr int kDefaultL2Prefetch = 0;  // streaming decode: heads prefetched into L2 ahead
+// kda_decode_step with FP32 state prefetches two heads into L2 beyond the
+// ring from 768 to 2048 heads (measured on the 34-layer stack at 64 heads:
+// M = 12 / 16 / 24 / 32 1.5 / 3.1 / 2.6 / 1.2 % faster; equal or slower at
+// M <= 8 and M >= 40, and for the fused step and BF16 state)
+constexpr int kL2PrefetchMid = 2, kL2PrefetchMinHeads = 768, kL2PrefetchMaxHeads = 2048;
 constexpr int kDefaultGroups = 2;      // streaming decode: consumer groups per CTA (FP32 state)
 constexpr int kDefaultGroupsBf16 = 4;  // BF16 state: four groups of four warps, state packed
 
